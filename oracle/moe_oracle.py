@@ -1,0 +1,290 @@
+"""fp64 CPU oracle of one dropless MoE layer, forward and backward.
+
+TEST INFRASTRUCTURE: this module is the independent reference the CUDA path is
+checked against.  It is imported only by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``; the library never calls it.
+
+Sources (web pages on dropless MoE training; none of them prints formulas, so
+each step below is the plainest reading of the text):
+
+* routing = softmax -> top-k selection -> mask, as one fused step
+  ("MoE operator optimisation: routing hardware acceleration and zero-copy
+  communication", gtnt.cn, section 2.1); the router network stays FP32
+  (same page, section 4.2);
+* dropless: every token copy is kept, no capacity and no padding (Pangu Ultra
+  MoE tech-report article, rjtj.cn, the dropless vs drop-and-pad comparison);
+* rearrange / un-rearrange of token copies into expert-contiguous order
+  (Huawei MoE training-operator article, feedman.me, section "Vector operator
+  (VectorSort)", Fig. 3);
+* layer output = weighted sum of the routed experts plus the shared expert
+  (rjtj.cn article, the shared/routed contribution analysis; one shared
+  expert per the reportify Pangu Ultra MoE summary);
+* backward with the expert dW and dX computed separately (rjtj.cn article,
+  adaptive-pipe overlap section; MindSpore DeepSeek-V3 page, section 01.2).
+
+Readings taken where the pages are silent (the layer contract):
+
+* top-k: the k largest scores, in descending order, equal scores resolved
+  toward the lower expert index;
+* gates: softmax over all E experts, picked at the top-k and renormalised over
+  them, which equals ``exp(s_e - m) / sum_{i in top-k} exp(s_i - m)``; no
+  routed scaling factor;
+* order of the copies inside an expert segment: stable in the flattened copy
+  index ``q = t*k + j``, i.e. ascending token;
+* expert FFN: SwiGLU ``(silu(x W1^T) * (x W3^T)) W2^T`` with no biases,
+  ``silu(a) = a / (1 + exp(-a))``;
+* shared experts are added with weight 1 and are not gated;
+* a per-expert score bias is a constant added before both selection and
+  gating; it has no gradient;
+* the top-k indices are constants of the backward (not differentiated).
+
+Every floating-point value here is fp64, except the selection scores when the
+caller passes fp32 logits: the top-k decision is then taken on the fp32 values
+themselves (and ``logits + bias`` is formed with one fp32 rounding, as the
+device does), because a decision that floating point makes must be made in the
+same precision on both sides.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "silu", "silu_grad", "router_logits", "selection_scores", "route_topk",
+    "expert_counts", "expert_offsets", "permutation", "swiglu_rows",
+    "layer_forward", "layer_backward", "router_backward", "as_f64",
+]
+
+
+def as_f64(t):
+    """Exact upcast of a torch tensor / numpy array (fp32 or bf16) to fp64 numpy."""
+    if t is None:
+        return None
+    if hasattr(t, "detach"):
+        import torch  # local import: the oracle itself only needs numpy
+        return t.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def silu(a):
+    return a / (1.0 + np.exp(-a))
+
+
+def silu_grad(a):
+    s = 1.0 / (1.0 + np.exp(-a))
+    return s * (1.0 + a * (1.0 - s))
+
+
+def router_logits(x, w_r):
+    """Router scores ``L = x W_r`` ([T, d] x [d, E]) in fp64."""
+    return np.asarray(x, np.float64) @ np.asarray(w_r, np.float64)
+
+
+def selection_scores(logits, bias=None):
+    """Scores the top-k compares.
+
+    fp32 logits (the device's own) keep fp32 and the bias is added with one
+    fp32 rounding; fp64 logits stay fp64.
+    """
+    logits = np.asarray(logits)
+    if logits.dtype == np.float32:
+        if bias is None:
+            return logits.copy()
+        return (logits + np.asarray(bias, np.float32)[None, :]).astype(np.float32)
+    s = np.asarray(logits, np.float64)
+    if bias is not None:
+        s = s + np.asarray(bias, np.float64)[None, :]
+    return s
+
+
+def route_topk(scores, k):
+    """Top-k selection and renormalised softmax gates.
+
+    Returns ``idx [T, k]`` (int64; descending score, lower index first on equal
+    scores) and ``w [T, k]`` (fp64, sums to 1 per row).
+    """
+    scores = np.asarray(scores)
+    assert np.all(np.isfinite(scores)), "router scores must be finite"
+    T, E = scores.shape
+    assert 1 <= k <= E
+    # A stable sort of the negated scores keeps equal scores in ascending
+    # expert order; negation is exact in any binary float format.
+    order = np.argsort(-scores, axis=1, kind="stable")
+    idx = order[:, :k].astype(np.int64)
+    s = np.take_along_axis(scores, idx, axis=1).astype(np.float64)
+    m = s[:, :1]  # the top-1 score is the row maximum
+    ex = np.exp(s - m)
+    w = ex / ex.sum(axis=1, keepdims=True)
+    return idx, w
+
+
+def expert_counts(idx, E):
+    return np.bincount(np.asarray(idx).reshape(-1), minlength=E).astype(np.int64)
+
+
+def expert_offsets(counts):
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+
+
+def permutation(idx, E):
+    """Stable counting sort of the copies ``q = t*k + j`` by expert.
+
+    Returns ``dest [T*k]`` (position of copy q in the expert-contiguous order)
+    and ``row_src [T*k]`` (token whose row sits at each position).
+    """
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    flat = idx.reshape(-1)
+    offsets = expert_offsets(expert_counts(idx, E))
+    fill = offsets[:-1].copy()
+    dest = np.empty(T * k, np.int64)
+    for q in range(T * k):          # ascending q: stable by construction
+        e = flat[q]
+        dest[q] = fill[e]
+        fill[e] += 1
+    row_src = np.empty(T * k, np.int64)
+    row_src[dest] = np.arange(T * k) // k
+    return dest, row_src
+
+
+def swiglu_rows(X, w13, w2):
+    """One expert on a block of rows: returns ``Z = [a | b]``, ``h``, ``Y``.
+
+    ``w13`` is ``[2f, d]`` (gate rows first, then up rows), ``w2`` is ``[d, f]``.
+    """
+    X = np.asarray(X, np.float64)
+    w13 = np.asarray(w13, np.float64)
+    w2 = np.asarray(w2, np.float64)
+    f = w13.shape[0] // 2
+    Z = X @ w13.T
+    a, b = Z[:, :f], Z[:, f:]
+    h = silu(a) * b
+    Y = h @ w2.T
+    return Z, h, Y
+
+
+def layer_forward(x, idx, w, w13, w2, ws13=None, ws2=None):
+    """Dropless MoE forward on fp64 inputs.
+
+    ``x [T, d]``, ``idx/w [T, k]`` from :func:`route_topk`, ``w13 [E, 2f, d]``,
+    ``w2 [E, d, f]``, shared ``ws13 [S, 2f_s, d]``, ``ws2 [S, d, f_s]``.
+    Returns a dict with ``y`` and every saved intermediate in the permuted
+    order (``x_perm``, ``z``, ``h``, ``y_perm``), the shared parts
+    (``z_sh[s]``, ``h_sh[s]``, ``y_sh``) and the routing bookkeeping.
+    """
+    x = np.asarray(x, np.float64)
+    T, d = x.shape
+    E = w13.shape[0]
+    k = idx.shape[1]
+    counts = expert_counts(idx, E)
+    offsets = expert_offsets(counts)
+    dest, row_src = permutation(idx, E)
+    x_perm = x[row_src]
+    f = w13.shape[1] // 2
+    z = np.zeros((T * k, 2 * f))
+    h = np.zeros((T * k, f))
+    y_perm = np.zeros((T * k, d))
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi > lo:
+            z[lo:hi], h[lo:hi], y_perm[lo:hi] = swiglu_rows(x_perm[lo:hi], w13[e], w2[e])
+    w_perm = np.empty(T * k)
+    w_perm[dest] = np.asarray(w, np.float64).reshape(-1)
+    y_sh = np.zeros((T, d))
+    z_sh, h_sh = [], []
+    S = 0 if ws13 is None else ws13.shape[0]
+    for s in range(S):
+        zs, hs, ys = swiglu_rows(x, ws13[s], ws2[s])
+        z_sh.append(zs)
+        h_sh.append(hs)
+        y_sh += ys
+    y = np.zeros((T, d))
+    for j in range(k):
+        y += np.asarray(w, np.float64)[:, j:j + 1] * y_perm[dest.reshape(T, k)[:, j]]
+    y += y_sh
+    return dict(y=y, counts=counts, offsets=offsets, dest=dest, row_src=row_src,
+                x_perm=x_perm, z=z, h=h, y_perm=y_perm, w_perm=w_perm,
+                z_sh=z_sh, h_sh=h_sh, y_sh=y_sh)
+
+
+def router_backward(w, dgate):
+    """Gradient of the loss w.r.t. the selected scores.
+
+    With ``w_j = exp(s_j) / sum_i exp(s_i)`` over the top-k,
+    ``dL_j = w_j * (dgate_j - sum_i w_i dgate_i)``; scores outside the top-k get 0.
+    """
+    w = np.asarray(w, np.float64)
+    dgate = np.asarray(dgate, np.float64)
+    return w * (dgate - np.sum(w * dgate, axis=1, keepdims=True))
+
+
+def layer_backward(x, idx, w, fwd, dy, w13, w2, ws13=None, ws2=None, w_r=None):
+    """Backward of :func:`layer_forward` given ``dy = dLoss/dy``.
+
+    Returns ``dx``, ``dw13``, ``dw2``, ``dws13``, ``dws2``, ``dgate [T, k]``,
+    ``dscores [T, E]`` (the gradient w.r.t. the router scores, i.e. the logits
+    when they are the input) and ``dw_r`` (when ``w_r`` is given; its term is
+    then also part of ``dx``).  The expert dX chain and the expert dW products
+    are separate computations, as on the pages.
+    """
+    x = np.asarray(x, np.float64)
+    dy = np.asarray(dy, np.float64)
+    T, d = x.shape
+    E = w13.shape[0]
+    k = idx.shape[1]
+    f = w13.shape[1] // 2
+    offsets, dest, row_src = fwd["offsets"], fwd["dest"], fwd["row_src"]
+    w_perm = fwd["w_perm"]
+    dy_perm = dy[row_src]
+    dgate_perm = np.zeros(T * k)
+    dz = np.zeros((T * k, 2 * f))
+    dx_perm = np.zeros((T * k, d))
+    dw13 = np.zeros(w13.shape)
+    dw2 = np.zeros(w2.shape)
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi == lo:
+            continue          # an expert without tokens keeps zero gradients
+        W13 = np.asarray(w13[e], np.float64)
+        W2 = np.asarray(w2[e], np.float64)
+        a, b = fwd["z"][lo:hi, :f], fwd["z"][lo:hi, f:]
+        h = fwd["h"][lo:hi]
+        D = dy_perm[lo:hi] @ W2                     # dLoss/d(h) before gating
+        dgate_perm[lo:hi] = np.sum(D * h, axis=1)
+        wr = w_perm[lo:hi, None]
+        dz_e = np.concatenate([wr * D * b * silu_grad(a), wr * D * silu(a)], axis=1)
+        dz[lo:hi] = dz_e
+        # dX chain
+        dx_perm[lo:hi] = dz_e @ W13
+        # dW products
+        dw2[e] = dy_perm[lo:hi].T @ (wr * h)
+        dw13[e] = dz_e.T @ fwd["x_perm"][lo:hi]
+    dx = np.zeros((T, d))
+    dmat = dest.reshape(T, k)
+    for j in range(k):
+        dx += dx_perm[dmat[:, j]]
+    S = 0 if ws13 is None else ws13.shape[0]
+    dws13 = np.zeros(ws13.shape) if S else None
+    dws2 = np.zeros(ws2.shape) if S else None
+    for s in range(S):
+        fs = ws13.shape[1] // 2
+        W13 = np.asarray(ws13[s], np.float64)
+        W2 = np.asarray(ws2[s], np.float64)
+        zs, hs = fwd["z_sh"][s], fwd["h_sh"][s]
+        a, b = zs[:, :fs], zs[:, fs:]
+        D = dy @ W2
+        dzs = np.concatenate([D * b * silu_grad(a), D * silu(a)], axis=1)
+        dx += dzs @ W13
+        dws2[s] = dy.T @ hs
+        dws13[s] = dzs.T @ x
+    dgate = dgate_perm[dest].reshape(T, k)
+    dsel = router_backward(w, dgate)
+    dscores = np.zeros((T, E))
+    np.put_along_axis(dscores, np.asarray(idx), dsel, axis=1)
+    dw_r = None
+    if w_r is not None:
+        w_r = np.asarray(w_r, np.float64)
+        dx += dscores @ w_r.T
+        dw_r = x.T @ dscores
+    return dict(dx=dx, dw13=dw13, dw2=dw2, dws13=dws13, dws2=dws2, dgate=dgate,
+                dscores=dscores, dw_r=dw_r, dz=dz, dx_perm=dx_perm,
+                dgate_perm=dgate_perm, dy_perm=dy_perm)
