@@ -1,0 +1,619 @@
+// bf16 grouped expert GEMMs on the 5th-generation tensor cores (sm_103a).
+//
+// One persistent, warp-specialised kernel per matmul kind (see grouped.cuh for the six):
+//   warp 0      TMA producer: 4-stage ring of 128x64 A and 256x64 B tiles (128-byte swizzle)
+//   warp 1      TMEM owner and single-thread tcgen05.mma issuer (M=128, N=256, K=16 steps,
+//               fp32 accumulators in TMEM, two accumulator buffers of 256 columns)
+//   warps 2..5  epilogue: tcgen05.ld -> fused math of the mode -> bf16 -> global memory
+// The tile schedule (groups = routed experts with ragged row counts, then shared experts)
+// is rebuilt by every CTA from the device-resident expert offsets, so nothing waits on the
+// host. Tiles of one expert run N-tile major / M-tile minor so concurrently running CTAs
+// share the expert's weight tile through L2.
+// Ragged edges: M tails read neighbouring rows (or the TMA zero fill) and are not stored;
+// ragged K (the dW products reduce over an expert's rows) zeroes the out-of-segment rows of
+// the A tile in shared memory before the last MMA of the tile.
+// Every mbarrier wait is bounded (1 s); on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT,
+// drains its TMA loads and MMAs, frees its TMEM and exits.
+#include <cuda.h>
+
+#include "grouped.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_BYTES = BN * BK * 2;          // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int kMaxGroups = 1024 + 8;
+constexpr int SLAB = 64 * 128;                // one 64-element-wide, 64-row swizzled slab
+
+struct TcParams {
+  CUtensorMap a0, a1, b0, b1;
+  GroupedArgs g;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tma2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                      int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                      int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, fixed version bits 46..47 = 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+         ((uint64_t)(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: D fp32, A/B bf16, M=128, N=256, majors per operand.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                     uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 fp32 -> 32 bf16 (RNE), stored as four 16-byte vectors.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
+    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
+    u.x = *reinterpret_cast<uint32_t*>(&h0);
+    u.y = *reinterpret_cast<uint32_t*>(&h1);
+    u.z = *reinterpret_cast<uint32_t*>(&h2);
+    u.w = *reinterpret_cast<uint32_t*>(&h3);
+    d4[q] = u;
+  }
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = __ldg(s4 + q);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      v[8 * q + 2 * i] = t.x;
+      v[8 * q + 2 * i + 1] = t.y;
+    }
+  }
+}
+
+template <int MODE> struct ModeTraits {
+  static constexpr bool a_mn = (MODE == DW2 || MODE == DW13);
+  static constexpr bool b_mn = (MODE == BWD2T || MODE == BWD1T || MODE == DW2 || MODE == DW13);
+  static constexpr bool k_tail = (MODE == DW2 || MODE == DW13);
+  static constexpr int bn_eff = (MODE == FWD1) ? BN / 2 : BN;
+};
+
+// ------------------------------------------------------------------ producer: TMA issue
+template <int MODE>
+__device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCoord& tc, int kb,
+                                                 uint32_t a_s, uint32_t b_s, uint32_t bar) {
+  const GroupedArgs& a = p.g;
+  const GroupGeom& G = tc.G;
+  const int m0 = tc.mi * BM;
+  const int k0 = kb * BK;
+  const int row0 = (int)G.row0;
+  const int T = (int)a.T;
+  if (MODE == FWD1) {
+    const int j0 = tc.ni * (BN / 2);
+    if (!G.shared) {
+      tma2d(a_s, &p.a0, bar, k0, row0 + m0);
+      tma3d(b_s, &p.b0, bar, k0, j0, G.e);
+      tma3d(b_s + B_BYTES / 2, &p.b0, bar, k0, a.f + j0, G.e);
+    } else {
+      tma2d(a_s, &p.a1, bar, k0, m0);
+      tma3d(b_s, &p.b1, bar, k0, j0, G.s);
+      tma3d(b_s + B_BYTES / 2, &p.b1, bar, k0, a.f_s + j0, G.s);
+    }
+  } else if (MODE == FWD2) {
+    const int n0 = tc.ni * BN;
+    if (!G.shared) {
+      tma2d(a_s, &p.a0, bar, k0, row0 + m0);
+      tma3d(b_s, &p.b0, bar, k0, n0, G.e);
+    } else {
+      const int kpb = a.f_s / BK, s = kb / kpb, kl = (kb - s * kpb) * BK;
+      tma2d(a_s, &p.a1, bar, kl, s * T + m0);
+      tma3d(b_s, &p.b1, bar, kl, n0, s);
+    }
+  } else if (MODE == BWD2T) {
+    const int n0 = tc.ni * BN;
+    if (!G.shared) {
+      tma2d(a_s, &p.a0, bar, k0, row0 + m0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b0, bar, n0 + 64 * i, k0, G.e);
+    } else {
+      tma2d(a_s, &p.a1, bar, k0, m0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b1, bar, n0 + 64 * i, k0, G.s);
+    }
+  } else if (MODE == BWD1T) {
+    const int n0 = tc.ni * BN;
+    if (!G.shared) {
+      tma2d(a_s, &p.a0, bar, k0, row0 + m0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b0, bar, n0 + 64 * i, k0, G.e);
+    } else {
+      const int kpb = 2 * a.f_s / BK, s = kb / kpb, kl = (kb - s * kpb) * BK;
+      tma2d(a_s, &p.a1, bar, kl, s * T + m0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b1, bar, n0 + 64 * i, kl, s);
+    }
+  } else {  // DW2 / DW13: A and B both MN-major, K runs over the group's rows
+    const int n0 = tc.ni * BN;
+    const int ka = G.shared ? ((MODE == DW13 ? G.s * T : 0) + k0) : row0 + k0;  // A rows
+    const int kbr = G.shared ? ((MODE == DW2 ? G.s * T : 0) + k0) : row0 + k0;  // B rows
+    const CUtensorMap* am = G.shared ? &p.a1 : &p.a0;
+    const CUtensorMap* bm = G.shared ? &p.b1 : &p.b0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) tma2d(a_s + i * SLAB, am, bar, m0 + 64 * i, ka);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tma2d(b_s + i * SLAB, bm, bar, n0 + 64 * i, kbr);
+  }
+}
+
+// ------------------------------------------------------------------ epilogues
+// Thread owns tile row r (TMEM lane); `acc` is the TMEM address of its lane, column 0.
+template <int MODE>
+__device__ __forceinline__ void epilogue_tile(const GroupedArgs& a, const TileCoord& tc, int r,
+                                              uint32_t acc) {
+  const GroupGeom& G = tc.G;
+  const int m0 = tc.mi * BM;
+  const int m = m0 + r;
+  const bool row_ok = m < G.M;
+  const int fw = G.shared ? a.f_s : a.f;
+  uint32_t u0[32], u1[32];
+  float v0[32], v1[32];
+
+  if (MODE == FWD1) {
+    const int j0 = tc.ni * (BN / 2);
+    __nv_bfloat16 *zr, *hr;
+    if (!G.shared) {
+      zr = (__nv_bfloat16*)a.z_out + (G.row0 + m) * (int64_t)(2 * a.f);
+      hr = (__nv_bfloat16*)a.h_out + (G.row0 + m) * (int64_t)a.f;
+    } else {
+      zr = (__nv_bfloat16*)a.z_sh_out + ((int64_t)G.s * a.T + m) * (2 * a.f_s);
+      hr = (__nv_bfloat16*)a.h_sh_out + ((int64_t)G.s * a.T + m) * a.f_s;
+    }
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      if (j0 + c >= fw) break;  // uniform across the warp
+      tmem_ld32(acc + c, u0);
+      tmem_ld32(acc + BN / 2 + c, u1);
+      tmem_ld_wait();
+      if (row_ok) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v0[i] = __uint_as_float(u0[i]);
+          v1[i] = __uint_as_float(u1[i]);
+        }
+        store_bf16x32(zr + j0 + c, v0);
+        store_bf16x32(zr + fw + j0 + c, v1);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v0[i] = silu_f(v0[i]) * v1[i];
+        store_bf16x32(hr + j0 + c, v0);
+      }
+    }
+  } else if (MODE == BWD2T) {
+    const int n0 = tc.ni * BN;
+    const __nv_bfloat16* zr;
+    __nv_bfloat16 *dzr, *hwr;
+    float w = 1.f;
+    if (!G.shared) {
+      zr = (const __nv_bfloat16*)a.z + (G.row0 + m) * (int64_t)(2 * a.f);
+      dzr = (__nv_bfloat16*)a.dz_out + (G.row0 + m) * (int64_t)(2 * a.f);
+      hwr = (__nv_bfloat16*)a.hw_out + (G.row0 + m) * (int64_t)a.f;
+      if (row_ok) w = __ldg(a.w_perm + G.row0 + m);
+    } else {
+      zr = (const __nv_bfloat16*)a.z_sh + ((int64_t)G.s * a.T + m) * (2 * a.f_s);
+      dzr = (__nv_bfloat16*)a.dz_sh_out + ((int64_t)G.s * a.T + m) * (2 * a.f_s);
+      hwr = (__nv_bfloat16*)a.hw_sh_out + ((int64_t)G.s * a.T + m) * a.f_s;
+    }
+    float dg = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      if (n0 + c >= fw) break;
+      tmem_ld32(acc + c, u0);
+      tmem_ld_wait();
+      if (row_ok) {
+        float za[32], zb[32];
+        load_bf16x32(zr + n0 + c, za);
+        load_bf16x32(zr + fw + n0 + c, zb);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float D = __uint_as_float(u0[i]);
+          const float av = za[i], bv = zb[i];
+          const float sg = 1.f / (1.f + expf(-av));
+          const float sl = av * sg;
+          const float hv = sl * bv;
+          dg = fmaf(D, hv, dg);
+          v0[i] = w * D * bv * (sg * (1.f + av * (1.f - sg)));
+          v1[i] = w * D * sl;
+          za[i] = w * hv;
+        }
+        store_bf16x32(dzr + n0 + c, v0);
+        store_bf16x32(dzr + fw + n0 + c, v1);
+        store_bf16x32(hwr + n0 + c, za);
+      }
+    }
+    if (!G.shared && row_ok) a.dgate_part[(int64_t)tc.ni * a.dgate_stride + G.row0 + m] = dg;
+  } else {
+    const int n0 = tc.ni * BN;
+    __nv_bfloat16* out;
+    switch (MODE) {
+      case FWD2:
+        out = G.shared ? (__nv_bfloat16*)a.y_sh + (int64_t)m * a.d
+                       : (__nv_bfloat16*)a.y_perm + (G.row0 + m) * (int64_t)a.d;
+        break;
+      case BWD1T:
+        out = G.shared ? (__nv_bfloat16*)a.dx_sh + (int64_t)m * a.d
+                       : (__nv_bfloat16*)a.dx_perm + (G.row0 + m) * (int64_t)a.d;
+        break;
+      case DW2:
+        out = G.shared ? (__nv_bfloat16*)a.dws2 + ((int64_t)G.s * a.d + m) * a.f_s
+                       : (__nv_bfloat16*)a.dw2 + ((int64_t)G.e * a.d + m) * a.f;
+        break;
+      default:  // DW13
+        out = G.shared ? (__nv_bfloat16*)a.dws13 + ((int64_t)G.s * 2 * a.f_s + m) * a.d
+                       : (__nv_bfloat16*)a.dw13 + ((int64_t)G.e * 2 * a.f + m) * a.d;
+        break;
+    }
+    const bool empty = ModeTraits<MODE>::k_tail && G.K == 0;  // dW of an expert without rows
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      if (n0 + c >= G.N) break;
+      if (!empty) {
+        tmem_ld32(acc + c, u0);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(u0[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v0[i] = 0.f;
+      }
+      if (row_ok) store_bf16x32(out + n0 + c, v0);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid_constant__ TcParams p) {
+  using TR = ModeTraits<MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], tail_bar, final_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_flag;
+  __shared__ int tile_start[kMaxGroups + 1];
+  __shared__ int warp_sums[32];
+
+  const GroupedArgs& a = p.g;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull_bar[b]), 1);
+      mbar_init(smem_u32(&tempty_bar[b]), 4);
+    }
+    mbar_init(smem_u32(&tail_bar), 1);
+    mbar_init(smem_u32(&final_bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_base_sh)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  build_tile_starts(a, MODE, BM, TR::bn_eff, tile_start, warp_sums);  // ends with __syncthreads
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+  const int ng = num_groups(MODE, a.E, a.S);
+  const int total = tile_start[ng];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0, tail_phase = 0;
+    uint32_t pending = 0;            // stages whose latest load may still be in flight
+    uint32_t pend_par = 0;           // parity of that load's phase, per stage
+    bool tail_pending = false;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM);
+      const int nkb = (tc.G.K + BK - 1) / BK;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const bool got = mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, &abort_flag,
+                                           a.err, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
+        const int rem = tc.G.K - kb * BK;
+        const bool tail = TR::k_tail && rem < BK;
+        const uint32_t fb = smem_u32(&full_bar[stage]);
+        if (!tail) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, fb);
+          }
+          pending |= 1u << stage;
+          pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+        } else {
+          const uint32_t tb = smem_u32(&tail_bar);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(tb, STAGE_BYTES);
+            issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, tb);
+          }
+          tail_pending = true;
+          const bool landed = mbar_wait_bounded(tb, tail_phase, &abort_flag, a.err, kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, landed)) { ok = false; break; }
+          tail_pending = false;
+          tail_phase ^= 1u;
+          // zero K rows [rem, 64) of both 64-wide slabs of the MN-major A tile
+          uint4* A4 = reinterpret_cast<uint4*>(smem + stage * STAGE_BYTES);
+          const int per_slab = (BK - rem) * 8;  // 16-byte chunks
+          for (int i = lane; i < 2 * per_slab; i += 32) {
+            const int sl = i / per_slab, j = i - sl * per_slab;
+            A4[sl * (SLAB / 16) + rem * 8 + j] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(fb);
+          pending &= ~(1u << stage);
+        }
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    // drain: no TMA load may still be writing shared memory when the CTA exits
+    for (int s = 0; s < STAGES; ++s)
+      if ((pending >> s) & 1u)
+        mbar_wait_bounded(smem_u32(&full_bar[s]), (pend_par >> s) & 1u, nullptr, a.err, kWaitLimitNs);
+    if (tail_pending) mbar_wait_bounded(smem_u32(&tail_bar), tail_phase, nullptr, a.err, kWaitLimitNs);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (one thread)
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(TR::a_mn, TR::b_mn);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool issued = false, ok = true;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+        const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM);
+        const int nkb = (tc.G.K + BK - 1) / BK;
+        const int b = it & 1;
+        if (!mbar_wait_bounded(smem_u32(&tempty_bar[b]), ((it >> 1) & 1) ^ 1, &abort_flag, a.err,
+                               kWaitLimitNs)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full_bar[stage]), phase, &abort_flag, a.err,
+                                 kWaitLimitNs)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = TR::a_mn ? sdesc(a_s + kk * 2048, SLAB, 1024) : sdesc(a_s + kk * 32, 16, 1024);
+            const uint64_t bd = TR::b_mn ? sdesc(b_s + kk * 2048, SLAB, 1024) : sdesc(b_s + kk * 32, 16, 1024);
+            umma(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          umma_commit(smem_u32(&empty_bar[stage]));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        if (nkb > 0) umma_commit(smem_u32(&tfull_bar[b]));
+        else mbar_arrive(smem_u32(&tfull_bar[b]));
+      }
+      if (issued) {  // all MMAs retired before TMEM is released
+        umma_commit(smem_u32(&final_bar));
+        mbar_wait_bounded(smem_u32(&final_bar), 0, nullptr, a.err, kWaitLimitNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue warps 2..5
+    const int lg = warp & 3;              // TMEM lane quarter this warp may access
+    const int r = lg * 32 + lane;         // tile row
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM);
+      const int b = it & 1;
+      const bool got = mbar_wait_bounded(smem_u32(&tfull_bar[b]), (it >> 1) & 1, &abort_flag,
+                                         a.err, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, got)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
+      tc_fence_after();
+      const uint32_t acc = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(b * BN);
+      epilogue_tile<MODE>(a, tc, r, acc);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[b]));
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host: tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 map over [rows][cols] (row pitch = cols elements), box {box_c, box_r}.
+bool map2d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_c, uint32_t box_r) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || ptr == nullptr || rows == 0 || cols == 0) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_c, box_r};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 map over [n][rows][cols], box {box_c, box_r, 1}.
+bool map3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t n, uint32_t box_c,
+           uint32_t box_r) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || ptr == nullptr || rows == 0 || cols == 0 || n == 0) return false;
+  const cuuint64_t dims[3] = {cols, rows, n};
+  const cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+  const cuuint32_t box[3] = {box_c, box_r, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+int launch_mode(TcParams& p, int num_sms, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(tc_grouped_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set = true;
+  }
+  tc_grouped_kernel<MODE><<<num_sms, NUM_THREADS, SMEM_BYTES, st>>>(p);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
+}  // namespace
+
+int tc_dgate_tiles(int f) { return (f + BN - 1) / BN; }
+
+int launch_tc_grouped(int mode, const GroupedArgs& g, int num_sms, cudaStream_t st) {
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.g = g;
+  const uint64_t Tk = (uint64_t)g.Tk, T = (uint64_t)g.T, ST = (uint64_t)g.S * g.T;
+  const uint64_t d = g.d, f = g.f, fs = g.f_s, E = g.E, S = g.S;
+  bool ok = true;
+  const bool sh = g.S > 0;
+  switch (mode) {
+    case FWD1:
+      ok = map2d(&p.a0, g.x_perm, d, Tk, 64, 128) && map3d(&p.b0, g.w13, d, 2 * f, E, 64, 128);
+      if (sh) ok = ok && map2d(&p.a1, g.x, d, T, 64, 128) && map3d(&p.b1, g.ws13, d, 2 * fs, S, 64, 128);
+      if (!ok) return MOE_ERR_CUDA;
+      return launch_mode<FWD1>(p, num_sms, st);
+    case FWD2:
+      ok = map2d(&p.a0, g.h, f, Tk, 64, 128) && map3d(&p.b0, g.w2, f, d, E, 64, 256);
+      if (sh) ok = ok && map2d(&p.a1, g.h_sh, fs, ST, 64, 128) && map3d(&p.b1, g.ws2, fs, d, S, 64, 256);
+      if (!ok) return MOE_ERR_CUDA;
+      return launch_mode<FWD2>(p, num_sms, st);
+    case BWD2T:
+      ok = map2d(&p.a0, g.dy_perm, d, Tk, 64, 128) && map3d(&p.b0, g.w2, f, d, E, 64, 64);
+      if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 128) && map3d(&p.b1, g.ws2, fs, d, S, 64, 64);
+      if (!ok) return MOE_ERR_CUDA;
+      return launch_mode<BWD2T>(p, num_sms, st);
+    case BWD1T:
+      ok = map2d(&p.a0, g.dz, 2 * f, Tk, 64, 128) && map3d(&p.b0, g.w13, d, 2 * f, E, 64, 64);
+      if (sh) ok = ok && map2d(&p.a1, g.dz_sh, 2 * fs, ST, 64, 128) && map3d(&p.b1, g.ws13, d, 2 * fs, S, 64, 64);
+      if (!ok) return MOE_ERR_CUDA;
+      return launch_mode<BWD1T>(p, num_sms, st);
+    case DW2:
+      ok = map2d(&p.a0, g.dy_perm, d, Tk, 64, 64) && map2d(&p.b0, g.hw, f, Tk, 64, 64);
+      if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 64) && map2d(&p.b1, g.hw_sh, fs, ST, 64, 64);
+      if (!ok) return MOE_ERR_CUDA;
+      return launch_mode<DW2>(p, num_sms, st);
+    default:
+      ok = map2d(&p.a0, g.dz, 2 * f, Tk, 64, 64) && map2d(&p.b0, g.x_perm, d, Tk, 64, 64);
+      if (sh) ok = ok && map2d(&p.a1, g.dz_sh, 2 * fs, ST, 64, 64) && map2d(&p.b1, g.x, d, T, 64, 64);
+      if (!ok) return MOE_ERR_CUDA;
+      return launch_mode<DW13>(p, num_sms, st);
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,164 @@
+// Grouped-GEMM problem description shared by the fp32 SIMT kernel and the bf16 tcgen05
+// kernel: the six matmul shapes of the expert FFN (forward, dX chain, dW products), the
+// groups they run over (routed experts with ragged row counts from `offsets`, then the
+// shared experts), and the device-built tile schedule.
+#pragma once
+
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// The six expert matmuls. Per group g (routed expert e, or shared expert s):
+//   FWD1  Z  = X  W13^T  [rows, 2f]  K = d        epilogue: h = silu(a)*b, store Z and h
+//   FWD2  Y  = h  W2^T   [rows, d]   K = f        (shared: one group, K = S*f_s concatenated)
+//   BWD2T D  = dY W2     [rows, f]   K = d        epilogue: dgate, dz, hw = w*h
+//   BWD1T dX = dz W13    [rows, d]   K = 2f       (shared: one group, K = S*2f_s concatenated)
+//   DW2   dW2  = dY^T hw [d, f]      K = rows
+//   DW13  dW13 = dz^T X  [2f, d]     K = rows
+enum Mode : int { FWD1 = 0, FWD2 = 1, BWD2T = 2, BWD1T = 3, DW2 = 4, DW13 = 5 };
+
+struct GroupedArgs {
+  int64_t T, Tk;
+  int d, E, k, f, S, f_s;
+  const int32_t* offsets;  // [E+1], device
+  // inputs
+  const void *x_perm, *x, *w13, *w2, *ws13, *ws2;
+  const void *h, *h_sh, *z, *z_sh, *dy_perm, *dy, *dz, *dz_sh, *hw, *hw_sh;
+  const float* w_perm;
+  // outputs
+  void *z_out, *z_sh_out, *h_out, *h_sh_out, *y_perm, *y_sh;
+  void *dz_out, *dz_sh_out, *hw_out, *hw_sh_out, *dx_perm, *dx_sh;
+  void *dw13, *dw2, *dws13, *dws2;
+  float* dgate_part;        // [n_tiles_f][Tk] per-N-tile partial sums of dgate (BWD2T)
+  int64_t dgate_stride;     // = Tk
+  int* err;
+};
+
+__host__ __device__ __forceinline__ int num_groups(int mode, int E, int S) {
+  if (mode == FWD2 || mode == BWD1T) return E + (S > 0 ? 1 : 0);
+  return E + S;
+}
+
+struct GroupGeom {
+  int64_t row0;   // first row of the group in the permuted/shared buffers
+  int64_t rows;   // rows of the group (token copies)
+  int M, N, K;    // matmul shape of the group
+  int e;          // routed expert index, or -1
+  int s;          // shared expert index (>= 0 for per-shared-expert groups), or -1
+  bool shared;
+};
+
+__device__ __forceinline__ GroupGeom group_geom(const GroupedArgs& a, int mode, int g) {
+  GroupGeom G;
+  G.shared = g >= a.E;
+  if (!G.shared) {
+    const int lo = __ldg(a.offsets + g), hi = __ldg(a.offsets + g + 1);
+    G.row0 = lo;
+    G.rows = hi - lo;
+    G.e = g;
+    G.s = -1;
+  } else {
+    G.row0 = 0;
+    G.rows = a.T;
+    G.e = -1;
+    G.s = (mode == FWD2 || mode == BWD1T) ? -1 : g - a.E;
+  }
+  const int fw = G.shared ? a.f_s : a.f;
+  const int rows32 = (int)G.rows;
+  switch (mode) {
+    case FWD1: G.M = rows32; G.N = fw; G.K = a.d; break;                 // N counts gate cols
+    case FWD2: G.M = rows32; G.N = a.d; G.K = G.shared ? a.S * a.f_s : a.f; break;
+    case BWD2T: G.M = rows32; G.N = fw; G.K = a.d; break;
+    case BWD1T: G.M = rows32; G.N = a.d; G.K = G.shared ? a.S * 2 * a.f_s : 2 * a.f; break;
+    case DW2: G.M = a.d; G.N = fw; G.K = rows32; break;
+    default: G.M = 2 * fw; G.N = a.d; G.K = rows32; break;             // DW13
+  }
+  return G;
+}
+
+// Block-wide exclusive scan of per-group tile counts into tile_start[0..ng] (shared memory).
+// Every thread of the block must call it. bn_eff = output columns one tile covers along N
+// (for FWD1 this is gate columns: a tile holds bn_eff gate and bn_eff up columns).
+__device__ __forceinline__ void build_tile_starts(const GroupedArgs& a, int mode, int bm,
+                                                  int bn_eff, int* tile_start, int* warp_sums) {
+  const int ng = num_groups(mode, a.E, a.S);
+  const int nt = blockDim.x;
+  const int per = (ng + nt - 1) / nt;
+  const int g0 = threadIdx.x * per;
+  int local = 0;
+  for (int i = 0; i < per; ++i) {
+    const int g = g0 + i;
+    if (g < ng) {
+      const GroupGeom G = group_geom(a, mode, g);
+      const int t = ((G.M + bm - 1) / bm) * ((G.N + bn_eff - 1) / bn_eff);
+      tile_start[g] = t;  // temporarily the count
+      local += t;
+    }
+  }
+  // exclusive scan of `local` across the block
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) warp_sums[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = (nt + 31) >> 5;
+    int v = lane < nw ? warp_sums[lane] : 0;
+    int vi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, vi, o);
+      if (lane >= o) vi += u;
+    }
+    if (lane < nw) warp_sums[lane] = vi - v;
+  }
+  __syncthreads();
+  int run = warp_sums[warp] + inc - local;
+  for (int i = 0; i < per; ++i) {
+    const int g = g0 + i;
+    if (g < ng) {
+      const int t = tile_start[g];
+      tile_start[g] = run;
+      run += t;
+    }
+  }
+  if (threadIdx.x == nt - 1) tile_start[ng] = run;
+  __syncthreads();
+}
+
+// Group owning linear tile `tile` (tile_start is non-decreasing; empty groups are skipped).
+__device__ __forceinline__ int find_group(const int* tile_start, int ng, int tile) {
+  int lo = 0, hi = ng;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_start[mid] <= tile) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+struct TileCoord {
+  GroupGeom G;
+  int g, mi, ni;
+};
+
+// Tiles of a group are ordered N-tile major, M-tile minor, so that CTAs working at the same
+// time on one expert share its weight tile through L2.
+__device__ __forceinline__ TileCoord decode_tile(const GroupedArgs& a, int mode, const int* tile_start,
+                                                 int ng, int tile, int bm) {
+  TileCoord c;
+  c.g = find_group(tile_start, ng, tile);
+  c.G = group_geom(a, mode, c.g);
+  const int local = tile - tile_start[c.g];
+  const int mt = (c.G.M + bm - 1) / bm;
+  c.ni = local / mt;
+  c.mi = local - c.ni * mt;
+  return c;
+}
+
+}  // namespace moe

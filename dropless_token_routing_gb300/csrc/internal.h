@@ -1,0 +1,78 @@
+// Host-side internals of the MoE library: workspace layout and kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+struct GroupedArgs;
+
+constexpr int kChunk = 64;        // tokens per permutation chunk (one 64-bit mask per expert)
+constexpr int kDwrSplit = 8;      // fixed row split of the router dW reduction
+constexpr int kMaxShared = 8;     // shared experts supported
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+
+inline size_t elt_bytes(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
+
+// Byte offsets of the workspace regions (each 256-byte aligned).
+struct WsLayout {
+  size_t err;          // int error word (+ padding)
+  size_t chunk_hist;   // [E][n_chunks] int32
+  size_t chunk_base;   // [E][n_chunks] int32
+  size_t local_rank;   // [T*k] int32
+  size_t dgate_part;   // [n_dgate_tiles][T*k] fp32
+  size_t dl_perm;      // [T*k] fp32  score gradient in permuted order
+  size_t dl_tok;       // [T*k] fp32  score gradient in token order
+  size_t dgate;        // [T*k] fp32
+  size_t w_rT;         // [E][d] fp32
+  size_t dwr_part;     // [kDwrSplit][E][d] fp32
+  size_t y_perm;       // [T*k, d]  (reused as dx_perm in the backward)
+  size_t y_sh;         // [T, d]
+  size_t dy_perm;      // [T*k, d]
+  size_t dz;           // [T*k, 2f]
+  size_t dz_sh;        // [S*T, 2f_s]
+  size_t hw;           // [T*k, f]
+  size_t hw_sh;        // [S*T, f_s]
+  size_t dx_sh;        // [T, d]
+  size_t total;
+  int64_t n_chunks;
+  int n_dgate_tiles;
+};
+
+WsLayout ws_layout(const moe_dims& d);
+
+// launchers (return the launch's cudaError_t)
+cudaError_t launch_router_logits(const void* x, const float* w_r, const moe_dims& dm, float* logits,
+                                 cudaStream_t st);
+cudaError_t launch_route_topk(const float* logits, const float* bias, int64_t T, int E, int k,
+                              int32_t* idx, float* w, int32_t* counts, int num_sms, cudaStream_t st);
+cudaError_t launch_route_bwd(const int32_t* idx, const float* w, const float* dgate_in,
+                             const float* dgate_part, int n_part, int64_t part_stride,
+                             const int32_t* dest, int64_t T, int E, int k, float* dgate_out,
+                             float* dlogits, float* dl_tok, float* dl_perm, cudaStream_t st);
+cudaError_t launch_permute(const void* x, const int32_t* idx, const float* topk_w, const moe_dims& dm,
+                           void* x_perm, int32_t* dest, int32_t* row_src, int32_t* offsets,
+                           float* w_perm, const WsLayout& L, uint8_t* ws, int* err, cudaStream_t st);
+cudaError_t launch_permute_rows(const void* x, const int32_t* dest, const moe_dims& dm, void* x_perm,
+                                cudaStream_t st);
+cudaError_t launch_combine(const void* y_perm, const int32_t* dest, const float* topk_w,
+                           const void* y_sh, const int32_t* idx, const float* dl_tok,
+                           const float* w_rT, const moe_dims& dm, void* y, cudaStream_t st);
+cudaError_t launch_transpose_f32(const float* in, int rows, int cols, float* out, cudaStream_t st);
+cudaError_t launch_dwr(const void* x, const int32_t* row_src, const float* dl_perm,
+                       const int32_t* offsets, const moe_dims& dm, float* part, float* dw_r,
+                       cudaStream_t st);
+cudaError_t launch_timeout_probe(int* err, uint64_t limit_ns, cudaStream_t st);
+
+int simt_dgate_tiles(int f);
+int tc_dgate_tiles(int f);
+cudaError_t launch_simt_grouped(int mode, const GroupedArgs& a, int num_sms, cudaStream_t st);
+// Returns MOE_OK or a negative status (tensor-map encoding can fail on the host).
+int launch_tc_grouped(int mode, const GroupedArgs& a, int num_sms, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,300 @@
+// VectorSort rearrange / un-rearrange: the stable expert permutation of token copies built
+// on the device (per-chunk expert bitmasks -> local ranks and chunk histograms -> scan ->
+// scatter), the row moves in 16-byte vectors, and the gate-weighted combine.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// ---------------------------------------------------------------- P1: chunk masks
+// One block per chunk of kChunk tokens, one thread per token. For every expert a 64-bit mask
+// of the chunk's tokens routed to it; a copy's rank inside the chunk is the popcount of the
+// mask below its token (tokens are distinct per expert, so this is the stable order).
+__global__ void __launch_bounds__(kChunk) permute_hist_kernel(
+    const int32_t* __restrict__ idx, int64_t T, int E, int k, int64_t n_chunks,
+    int32_t* __restrict__ chunk_hist, int32_t* __restrict__ local_rank, int* err) {
+  extern __shared__ uint32_t mask[];  // [E][2]
+  const int64_t c = blockIdx.x;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < 2 * E; i += kChunk) mask[i] = 0u;
+  __syncthreads();
+  const int64_t t = c * kChunk + tid;
+  const bool tok = t < T;
+  const int word = tid >> 5;
+  const uint32_t bit = 1u << (tid & 31);
+  if (tok) {
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[t * k + j];
+      bool ok = e >= 0 && e < E;
+      for (int jj = 0; jj < j && ok; ++jj) ok = idx[t * k + jj] != e;
+      if (ok) atomicOr(&mask[2 * e + word], bit);
+      else record_error(err, MOE_ERR_DEVICE_EXPERT_ID);
+    }
+  }
+  __syncthreads();
+  if (tok) {
+    const uint32_t below = bit - 1u;
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[t * k + j];
+      bool ok = e >= 0 && e < E;
+      for (int jj = 0; jj < j && ok; ++jj) ok = idx[t * k + jj] != e;
+      int r = -1;
+      if (ok) r = (word ? __popc(mask[2 * e]) : 0) + __popc(mask[2 * e + word] & below);
+      local_rank[t * k + j] = r;
+    }
+  }
+  for (int e = tid; e < E; e += kChunk)
+    chunk_hist[(int64_t)e * n_chunks + c] = __popc(mask[2 * e]) + __popc(mask[2 * e + 1]);
+}
+
+// ---------------------------------------------------------------- P2: scans
+// One block of 1024 threads. Warp w scans the chunk histograms of experts w, w+32, ...;
+// then the per-expert totals are scanned into offsets.
+__global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __restrict__ chunk_hist,
+                                                            int32_t* __restrict__ chunk_base,
+                                                            int64_t n_chunks, int E,
+                                                            int32_t* __restrict__ offsets) {
+  __shared__ int cnt[kMaxE];
+  __shared__ int wsum[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = warp; e < E; e += 32) {
+    int run = 0;
+    const int32_t* hrow = chunk_hist + (int64_t)e * n_chunks;
+    int32_t* brow = chunk_base + (int64_t)e * n_chunks;
+    for (int64_t c0 = 0; c0 < n_chunks; c0 += 32) {
+      const int64_t c = c0 + lane;
+      const int v = c < n_chunks ? hrow[c] : 0;
+      int inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+      }
+      if (c < n_chunks) brow[c] = run + inc - v;
+      run += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) cnt[e] = run;
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int v = e < E ? cnt[e] : 0;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += u;
+  }
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int s = wsum[lane];
+    int si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, si, o);
+      if (lane >= o) si += u;
+    }
+    wsum[lane] = si - s;
+  }
+  __syncthreads();
+  const int excl = wsum[warp] + inc - v;
+  if (e < E) offsets[e] = excl;
+  if (e == E - 1) offsets[E] = excl + v;
+}
+
+// ---------------------------------------------------------------- P3: scatter + row move
+// One warp per token: lanes j < k compute dest of copy j, then the row x[t] is read once in
+// 16-byte vectors and written to the k destination rows.
+template <typename T, int U>
+__device__ __forceinline__ void copy_row_to_dests(const T* __restrict__ src, T* __restrict__ dst,
+                                                  int d, int k, int dq, int lane) {
+  const int nvec = d / 8;
+  for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+    Vec8<T> val[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u;
+      if (v < nvec) val[u].load(src + (int64_t)v * 8);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int dj = __shfl_sync(0xffffffffu, dq, j);
+      if (dj < 0) continue;
+      T* drow = dst + (int64_t)dj * d;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < nvec) val[u].store(drow + (int64_t)v * 8);
+      }
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) permute_scatter_kernel(
+    const T* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
+    const int32_t* __restrict__ local_rank, const int32_t* __restrict__ chunk_base,
+    const int32_t* __restrict__ offsets, int64_t Tn, int d, int k, int64_t n_chunks,
+    T* __restrict__ x_perm, int32_t* __restrict__ dest, int32_t* __restrict__ row_src,
+    float* __restrict__ w_perm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < Tn; t += (int64_t)gridDim.x * nw) {
+    int dq = -1;
+    if (lane < k) {
+      const int64_t q = t * k + lane;
+      const int r = local_rank[q];
+      if (r >= 0) {
+        const int e = idx[q];
+        dq = offsets[e] + chunk_base[(int64_t)e * n_chunks + t / kChunk] + r;
+        row_src[dq] = (int32_t)t;
+        if (w_perm != nullptr) w_perm[dq] = topk_w[q];
+      }
+      dest[q] = dq;
+    }
+    copy_row_to_dests<T, 4>(x + t * d, x_perm, d, k, dq, lane);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) permute_rows_kernel(const T* __restrict__ x,
+                                                           const int32_t* __restrict__ dest,
+                                                           int64_t Tn, int d, int k,
+                                                           T* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < Tn; t += (int64_t)gridDim.x * nw) {
+    const int dq = lane < k ? dest[t * k + lane] : -1;
+    copy_row_to_dests<T, 4>(x + t * d, x_perm, d, k, dq, lane);
+  }
+}
+
+// ---------------------------------------------------------------- a4: combine
+// y[t] = sum_j w_j y_perm[dest_j] (+ y_sh[t]) (+ sum_j dl_j W_r^T[e_j]) in fp32, in that
+// order, rounded once. One warp per token, 8 elements per lane per step.
+template <typename T, bool ROUTER>
+__global__ void __launch_bounds__(256) combine_kernel(
+    const T* __restrict__ y_perm, const int32_t* __restrict__ dest, const float* __restrict__ topk_w,
+    const T* __restrict__ y_sh, const int32_t* __restrict__ idx, const float* __restrict__ dl_tok,
+    const float* __restrict__ w_rT, int64_t Tn, int d, int k, T* __restrict__ y) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int nvec = d / 8;
+  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < Tn; t += (int64_t)gridDim.x * nw) {
+    int dq = -1, eq = 0;
+    float wq = 0.f, gq = 0.f;
+    if (lane < k) {
+      const int64_t q = t * k + lane;
+      dq = dest[q];
+      wq = topk_w != nullptr ? topk_w[q] : 1.f;
+      if (ROUTER) {
+        eq = idx[q];
+        gq = dl_tok[q];
+      }
+    }
+    for (int v = lane; v < nvec; v += 32) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < k; ++j) {
+        const int dj = __shfl_sync(0xffffffffu, dq, j);
+        const float wj = __shfl_sync(0xffffffffu, wq, j);
+        if (dj < 0) continue;
+        Vec8<T> val;
+        val.load(y_perm + (int64_t)dj * d + (int64_t)v * 8);
+        float f[8];
+        val.to_float(f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+      }
+      if (y_sh != nullptr) {
+        Vec8<T> val;
+        val.load(y_sh + t * d + (int64_t)v * 8);
+        float f[8];
+        val.to_float(f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += f[i];
+      }
+      if (ROUTER) {
+        for (int j = 0; j < k; ++j) {
+          const int ej = __shfl_sync(0xffffffffu, eq, j);
+          const float gj = __shfl_sync(0xffffffffu, gq, j);
+          const float4* wr = reinterpret_cast<const float4*>(w_rT + (int64_t)ej * d + (int64_t)v * 8);
+          const float4 p0 = __ldg(wr), p1 = __ldg(wr + 1);
+          acc[0] = fmaf(gj, p0.x, acc[0]); acc[1] = fmaf(gj, p0.y, acc[1]);
+          acc[2] = fmaf(gj, p0.z, acc[2]); acc[3] = fmaf(gj, p0.w, acc[3]);
+          acc[4] = fmaf(gj, p1.x, acc[4]); acc[5] = fmaf(gj, p1.y, acc[5]);
+          acc[6] = fmaf(gj, p1.z, acc[6]); acc[7] = fmaf(gj, p1.w, acc[7]);
+        }
+      }
+      Vec8<T> out;
+      out.from_float(acc);
+      out.store(y + t * d + (int64_t)v * 8);
+    }
+  }
+}
+
+int64_t token_blocks(int64_t T, int num_per_block, int64_t cap) {
+  int64_t b = (T + num_per_block - 1) / num_per_block;
+  if (b > cap) b = cap;
+  return b < 1 ? 1 : b;
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const void* x, const int32_t* idx, const float* topk_w, const moe_dims& dm,
+                           void* x_perm, int32_t* dest, int32_t* row_src, int32_t* offsets,
+                           float* w_perm, const WsLayout& L, uint8_t* ws, int* err, cudaStream_t st) {
+  int32_t* chunk_hist = reinterpret_cast<int32_t*>(ws + L.chunk_hist);
+  int32_t* chunk_base = reinterpret_cast<int32_t*>(ws + L.chunk_base);
+  int32_t* local_rank = reinterpret_cast<int32_t*>(ws + L.local_rank);
+  permute_hist_kernel<<<(unsigned)L.n_chunks, kChunk, sizeof(uint32_t) * 2 * dm.E, st>>>(
+      idx, dm.T, dm.E, dm.k, L.n_chunks, chunk_hist, local_rank, err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  permute_scan_kernel<<<1, 1024, 0, st>>>(chunk_hist, chunk_base, L.n_chunks, dm.E, offsets);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const unsigned blocks = (unsigned)token_blocks(dm.T, 8, 1 << 20);
+  if (dm.dtype == MOE_F32)
+    permute_scatter_kernel<float><<<blocks, 256, 0, st>>>(
+        (const float*)x, idx, topk_w, local_rank, chunk_base, offsets, dm.T, dm.d, dm.k, L.n_chunks,
+        (float*)x_perm, dest, row_src, w_perm);
+  else
+    permute_scatter_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+        (const __nv_bfloat16*)x, idx, topk_w, local_rank, chunk_base, offsets, dm.T, dm.d, dm.k,
+        L.n_chunks, (__nv_bfloat16*)x_perm, dest, row_src, w_perm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_rows(const void* x, const int32_t* dest, const moe_dims& dm, void* x_perm,
+                                cudaStream_t st) {
+  const unsigned blocks = (unsigned)token_blocks(dm.T, 8, 1 << 20);
+  if (dm.dtype == MOE_F32)
+    permute_rows_kernel<float><<<blocks, 256, 0, st>>>((const float*)x, dest, dm.T, dm.d, dm.k,
+                                                       (float*)x_perm);
+  else
+    permute_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
+        (const __nv_bfloat16*)x, dest, dm.T, dm.d, dm.k, (__nv_bfloat16*)x_perm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y_perm, const int32_t* dest, const float* topk_w,
+                           const void* y_sh, const int32_t* idx, const float* dl_tok,
+                           const float* w_rT, const moe_dims& dm, void* y, cudaStream_t st) {
+  const unsigned blocks = (unsigned)token_blocks(dm.T, 8, 1 << 20);
+  const bool router = w_rT != nullptr;
+  if (dm.dtype == MOE_F32) {
+    if (router)
+      combine_kernel<float, true><<<blocks, 256, 0, st>>>((const float*)y_perm, dest, topk_w,
+          (const float*)y_sh, idx, dl_tok, w_rT, dm.T, dm.d, dm.k, (float*)y);
+    else
+      combine_kernel<float, false><<<blocks, 256, 0, st>>>((const float*)y_perm, dest, topk_w,
+          (const float*)y_sh, idx, dl_tok, w_rT, dm.T, dm.d, dm.k, (float*)y);
+  } else {
+    if (router)
+      combine_kernel<__nv_bfloat16, true><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y_perm, dest,
+          topk_w, (const __nv_bfloat16*)y_sh, idx, dl_tok, w_rT, dm.T, dm.d, dm.k, (__nv_bfloat16*)y);
+    else
+      combine_kernel<__nv_bfloat16, false><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y_perm, dest,
+          topk_w, (const __nv_bfloat16*)y_sh, idx, dl_tok, w_rT, dm.T, dm.d, dm.k, (__nv_bfloat16*)y);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

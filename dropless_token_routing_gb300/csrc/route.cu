@@ -1,0 +1,336 @@
+// Router: fp32 scores (a0), fused softmax -> top-k -> gates -> counts (a1), and the router
+// backward (score gradient of the renormalised softmax, router dW).
+#include <float.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// ---------------------------------------------------------------- a0: L = x W_r (fp32 FMA)
+constexpr int RBM = 64, RBN = 64, RBK = 16;
+
+template <typename TX>
+__global__ void __launch_bounds__(256) router_logits_kernel(const TX* __restrict__ x,
+                                                            const float* __restrict__ w_r,
+                                                            float* __restrict__ L, int64_t T,
+                                                            int d, int E) {
+  __shared__ float As[RBK][RBM + 4];
+  __shared__ float Bs[RBK][RBN + 4];
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int64_t m0 = (int64_t)blockIdx.y * RBM;
+  const int n0 = blockIdx.x * RBN;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < d; k0 += RBK) {
+    {  // A: 64 rows x 16 k, 4 consecutive k per thread (d is a multiple of 8)
+      const int r = tid >> 2, kq = (tid & 3) * 4;
+      const int64_t gm = m0 + r;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (gm < T && k0 + kq < d) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = to_f32(x[gm * d + k0 + kq + i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) As[kq + i][r] = v[i];
+    }
+    {  // B: 16 k x 64 experts
+      const int kk = tid >> 4, nq = (tid & 15) * 4;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int n = n0 + nq + i;
+        Bs[kk][nq + i] = (k0 + kk < d && n < E) ? w_r[(int64_t)(k0 + kk) * E + n] : 0.f;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < RBK; ++kk) {
+      const float4 a4 = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+      const float4 b4 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+      const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+      const float bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t gm = m0 + ty * 4 + i;
+    if (gm >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n < E) L[gm * E + n] = acc[i][j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- a1: fused route
+// One warp per token. Lane l holds the scores of experts l, l+32, ... (V per lane).
+// k rounds of a warp arg-max under the order (score descending, index ascending).
+template <int V>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits,
+                                                         const float* __restrict__ bias, int64_t T,
+                                                         int E, int k, int32_t* __restrict__ idx,
+                                                         float* __restrict__ w,
+                                                         int32_t* __restrict__ counts) {
+  extern __shared__ int hist[];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < T; t += (int64_t)gridDim.x * nw) {
+    float v[V];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        float s = __ldg(logits + t * E + e);
+        if (bias != nullptr) s = s + __ldg(bias + e);   // one fp32 rounding
+        v[i] = s;
+      } else {
+        v[i] = -FLT_MAX;
+        taken |= 1u << i;
+      }
+    }
+    float my_v = 0.f;
+    int my_i = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -FLT_MAX;
+      int bi = 0x7fffffff;
+      bool have = false;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        if (!((taken >> i) & 1u) && (!have || v[i] > bv)) {  // ascending index: ties keep lower
+          bv = v[i];
+          bi = lane + 32 * i;
+          have = true;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        const int oh = __shfl_xor_sync(0xffffffffu, (int)have, o);
+        if (oh && (!have || ov > bv || (ov == bv && oi < bi))) {
+          bv = ov;
+          bi = oi;
+          have = true;
+        }
+      }
+      if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_v = bv;
+        my_i = bi;
+      }
+    }
+    const float m = __shfl_sync(0xffffffffu, my_v, 0);   // top-1 = row maximum
+    const float ex = lane < k ? expf(my_v - m) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < k) {
+      idx[t * k + lane] = my_i;
+      w[t * k + lane] = ex / sum;
+      atomicAdd(&hist[my_i], 1);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    if (hist[i] != 0) atomicAdd(counts + i, hist[i]);
+}
+
+// ---------------------------------------------------------------- router backward
+// dl_j = w_j (dgate_j - sum_i w_i dgate_i) on the top-k, 0 elsewhere. One warp per token.
+// dgate comes either directly or as the sum of per-N-tile partials at row dest[q].
+__global__ void __launch_bounds__(256) route_bwd_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ w, const float* __restrict__ dgate_in,
+    const float* __restrict__ dgate_part, int n_part, int64_t part_stride,
+    const int32_t* __restrict__ dest, int64_t T, int E, int k, float* __restrict__ dgate_out,
+    float* __restrict__ dlogits, float* __restrict__ dl_tok, float* __restrict__ dl_perm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < T; t += (int64_t)gridDim.x * nw) {
+    const int64_t q = t * k + lane;
+    float dg = 0.f, wj = 0.f;
+    int dq = -1, e = -1;
+    if (lane < k) {
+      wj = w[q];
+      e = idx[q];
+      if (dest != nullptr) dq = dest[q];
+      if (dgate_in != nullptr) {
+        dg = dgate_in[q];
+      } else if (dq >= 0) {
+        for (int p = 0; p < n_part; ++p) dg += dgate_part[(int64_t)p * part_stride + dq];
+      }
+      if (dgate_out != nullptr) dgate_out[q] = dg;
+    }
+    float s = wj * dg;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float dl = wj * (dg - s);
+    if (dlogits != nullptr) {
+      for (int c = lane; c < E; c += 32) dlogits[t * E + c] = 0.f;
+      __syncwarp();
+      if (lane < k && e >= 0 && e < E) dlogits[t * E + e] = dl;
+    }
+    if (lane < k) {
+      if (dl_tok != nullptr) dl_tok[q] = dl;
+      if (dl_perm != nullptr && dq >= 0) dl_perm[dq] = dl;
+    }
+  }
+}
+
+// out[c][r] = in[r][c] for an fp32 [rows][cols] matrix.
+__global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int cols,
+                                     float* __restrict__ out) {
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    tile[i][threadIdx.x] = (r < rows && c < cols) ? in[(int64_t)r * cols + c] : 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (c < cols && r < rows) out[(int64_t)c * rows + r] = tile[threadIdx.x][i];
+  }
+}
+
+// Router dW: dW_r[:, e] = sum over the copies routed to e of dl * x[token]. Deterministic:
+// each expert's rows are cut into kDwrSplit fixed slices, each slice summed in row order,
+// then the slices are summed in slice order.
+template <typename TX>
+__global__ void __launch_bounds__(256) dwr_partial_kernel(const TX* __restrict__ x,
+                                                          const int32_t* __restrict__ row_src,
+                                                          const float* __restrict__ dl_perm,
+                                                          const int32_t* __restrict__ offsets, int d,
+                                                          int E, float* __restrict__ part) {
+  const int e = blockIdx.x / kDwrSplit, sl = blockIdx.x % kDwrSplit;
+  const int64_t lo = offsets[e], n = offsets[e + 1] - lo;
+  const int64_t r0 = lo + n * sl / kDwrSplit, r1 = lo + n * (sl + 1) / kDwrSplit;
+  const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  if (c >= d) return;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int64_t r = r0; r < r1; ++r) {
+    const int64_t t = row_src[r];
+    const float g = dl_perm[r];
+    const TX* xr = x + t * d + c;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = fmaf(g, to_f32(xr[i]), acc[i]);
+  }
+  float* out = part + ((int64_t)sl * E + e) * d + c;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) out[i] = acc[i];
+}
+
+// dw_r[c][e] = sum_sl part[sl][e][c] (slice order), through a 32x32 transpose tile.
+__global__ void dwr_reduce_kernel(const float* __restrict__ part, int d, int E,
+                                  float* __restrict__ dw_r) {
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int e = e0 + i, c = c0 + threadIdx.x;
+    float s = 0.f;
+    if (e < E && c < d)
+      for (int sl = 0; sl < kDwrSplit; ++sl) s += part[((int64_t)sl * E + e) * d + c];
+    tile[i][threadIdx.x] = s;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i, e = e0 + threadIdx.x;
+    if (c < d && e < E) dw_r[(int64_t)c * E + e] = tile[threadIdx.x][i];
+  }
+}
+
+// A bounded wait on a barrier nothing completes: exercises the timeout path end to end.
+__global__ void timeout_probe_kernel(int* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, err, limit_ns);
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_router_logits(const void* x, const float* w_r, const moe_dims& dm, float* logits,
+                                 cudaStream_t st) {
+  const dim3 grid((dm.E + RBN - 1) / RBN, (unsigned)((dm.T + RBM - 1) / RBM)), block(256);
+  if (dm.dtype == MOE_F32)
+    router_logits_kernel<float><<<grid, block, 0, st>>>((const float*)x, w_r, logits, dm.T, dm.d, dm.E);
+  else
+    router_logits_kernel<__nv_bfloat16><<<grid, block, 0, st>>>((const __nv_bfloat16*)x, w_r, logits,
+                                                                dm.T, dm.d, dm.E);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_topk(const float* logits, const float* bias, int64_t T, int E, int k,
+                              int32_t* idx, float* w, int32_t* counts, int num_sms, cudaStream_t st) {
+  const int threads = 256, wpb = threads / 32;
+  int64_t blocks = (T + wpb - 1) / wpb;
+  if (blocks > 4 * num_sms) blocks = 4 * num_sms;
+  if (blocks < 1) blocks = 1;
+  const size_t sm = sizeof(int) * E;
+  const int V = (E + 31) / 32;
+#define MOE_ROUTE_CASE(VV)                                                                   \
+  route_topk_kernel<VV><<<(unsigned)blocks, threads, sm, st>>>(logits, bias, T, E, k, idx, w, \
+                                                               counts);
+  if (V <= 1) { MOE_ROUTE_CASE(1) }
+  else if (V <= 2) { MOE_ROUTE_CASE(2) }
+  else if (V <= 4) { MOE_ROUTE_CASE(4) }
+  else if (V <= 8) { MOE_ROUTE_CASE(8) }
+  else if (V <= 16) { MOE_ROUTE_CASE(16) }
+  else { MOE_ROUTE_CASE(32) }
+#undef MOE_ROUTE_CASE
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_bwd(const int32_t* idx, const float* w, const float* dgate_in,
+                             const float* dgate_part, int n_part, int64_t part_stride,
+                             const int32_t* dest, int64_t T, int E, int k, float* dgate_out,
+                             float* dlogits, float* dl_tok, float* dl_perm, cudaStream_t st) {
+  const int threads = 256, wpb = threads / 32;
+  int64_t blocks = (T + wpb - 1) / wpb;
+  if (blocks > 65535) blocks = 65535;
+  route_bwd_kernel<<<(unsigned)blocks, threads, 0, st>>>(idx, w, dgate_in, dgate_part, n_part,
+                                                         part_stride, dest, T, E, k, dgate_out,
+                                                         dlogits, dl_tok, dl_perm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_f32(const float* in, int rows, int cols, float* out, cudaStream_t st) {
+  const dim3 grid((cols + 31) / 32, (rows + 31) / 32), block(32, 8);
+  transpose_f32_kernel<<<grid, block, 0, st>>>(in, rows, cols, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dwr(const void* x, const int32_t* row_src, const float* dl_perm,
+                       const int32_t* offsets, const moe_dims& dm, float* part, float* dw_r,
+                       cudaStream_t st) {
+  const dim3 g1(dm.E * kDwrSplit, (dm.d + 1023) / 1024), b1(256);
+  if (dm.dtype == MOE_F32)
+    dwr_partial_kernel<float><<<g1, b1, 0, st>>>((const float*)x, row_src, dl_perm, offsets, dm.d, dm.E, part);
+  else
+    dwr_partial_kernel<__nv_bfloat16><<<g1, b1, 0, st>>>((const __nv_bfloat16*)x, row_src, dl_perm,
+                                                         offsets, dm.d, dm.E, part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const dim3 g2((dm.d + 31) / 32, (dm.E + 31) / 32), b2(32, 8);
+  dwr_reduce_kernel<<<g2, b2, 0, st>>>(part, dm.d, dm.E, dw_r);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_timeout_probe(int* err, uint64_t limit_ns, cudaStream_t st) {
+  timeout_probe_kernel<<<1, 32, 0, st>>>(err, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

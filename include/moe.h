@@ -1,0 +1,240 @@
+/*
+ * moe.h -- C ABI of the dropless Mixture-of-Experts layer hot path (GB300, sm_103a).
+ *
+ * The layer (per token t of x [T, d]):
+ *   router   s_t    = x_t W_r (+ b)                           fp32 scores over E experts
+ *   route    S_t    = the k largest s_t, descending, ties -> lower expert index
+ *            w_t,j  = exp(s_t,e_j) / sum_{i in S_t} exp(s_t,e_i)   (softmax renormalised on the top-k)
+ *   permute  every copy q = t*k + j goes to row dest[q] of an expert-contiguous buffer,
+ *            experts in ascending order, copies of one expert in ascending q (stable)
+ *   experts  Y_q    = (silu(x_t W1_e^T) * (x_t W3_e^T)) W2_e^T   SwiGLU, one grouped GEMM
+ *   combine  y_t    = sum_j w_t,j Y_dest[t*k+j] + sum_s SwiGLU_s(x_t)   (shared experts, weight 1)
+ *   backward dX chain and dW products computed by separate calls.
+ * Sources: routing as fused softmax -> top-k -> mask and an FP32 router ("MoE operator
+ * optimisation: routing hardware acceleration and zero-copy communication", sections 2.1
+ * and 4.2); dropless routing (Pangu Ultra MoE tech-report article, dropless vs
+ * drop-and-pad); rearrange / un-rearrange of token copies (Huawei MoE training-operator
+ * article, "VectorSort", Fig. 3) with dispatch preprocessing that never waits on the device
+ * (same article, sync elimination, Fig. 4); grouped matmul over experts (MindSpore
+ * DeepSeek-V3 page, section 02.1); shared + routed weighted sum (Pangu Ultra MoE article,
+ * contribution analysis); expert dW and dX computed separately (Pangu Ultra MoE article,
+ * adaptive pipe overlap; MindSpore page, section 01.2).
+ *
+ * Conventions of every call:
+ *  - Tensor pointers are DEVICE pointers owned by the caller, row-major, 16-byte aligned.
+ *    The library allocates and frees nothing.
+ *  - Calls are asynchronous on `stream` and never synchronise (except moe_get_device_error).
+ *  - Activations and expert weights are fp32 (MOE_F32) or bf16 (MOE_BF16) as dims->dtype says;
+ *    router weights, scores, gates, dgate and score gradients are always fp32; indices int32.
+ *  - Expert weights are K-major: W13 [E][2f][d] (gate rows 0..f-1, up rows f..2f-1),
+ *    W2 [E][d][f]; shared experts Ws13 [S][2f_s][d], Ws2 [S][d][f_s]. Gradients share layouts.
+ *  - Buffers with "routed rows" have T*k rows in the permuted (expert-contiguous) order;
+ *    "shared rows" have S*T rows, shared expert s owning rows s*T .. s*T+T-1.
+ *  - Return value: MOE_OK, or a negative status for an argument error detected on the host
+ *    (nothing is launched then), or MOE_ERR_LAUNCH / MOE_ERR_CUDA for a CUDA error.
+ *  - Errors found on the device (an expert id out of range, a bounded wait that ran out) are
+ *    recorded in an error word inside the workspace; moe_get_device_error reads and clears it.
+ *  - T == 0 is a valid no-op.
+ *  - bf16 needs d, f, f_s multiples of 64; fp32 needs multiples of 8. E <= 1024, 1 <= k <= min(E, 32).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_NULL_POINTER = -1,        /* a required pointer is NULL */
+  MOE_ERR_MISALIGNED = -2,          /* a pointer is not 16-byte aligned (workspace: 256) */
+  MOE_ERR_BAD_DIMS = -3,            /* T < 0, d/f/f_s not a multiple of the dtype's unit, E out of range */
+  MOE_ERR_BAD_TOPK = -4,            /* k < 1, k > E or k > 32 */
+  MOE_ERR_UNSUPPORTED_DTYPE = -5,   /* dtype is neither MOE_F32 nor MOE_BF16 */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -6, /* ws_bytes < moe_workspace_bytes(dims) */
+  MOE_ERR_LAUNCH = -7,              /* a kernel launch failed */
+  MOE_ERR_CUDA = -8,                /* another CUDA runtime/driver call failed */
+  MOE_ERR_UNSUPPORTED_DEVICE = -9,  /* bf16 grouped GEMM needs an sm_103 (GB300) device */
+  MOE_ERR_DEVICE_EXPERT_ID = -100,  /* device: expert id outside [0, E) or repeated in a row */
+  MOE_ERR_DEVICE_TIMEOUT = -101     /* device: a bounded wait ran out */
+};
+
+enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 };
+
+typedef struct moe_dims {
+  int64_t T;     /* tokens */
+  int32_t d;     /* hidden size */
+  int32_t E;     /* routed experts */
+  int32_t k;     /* experts per token */
+  int32_t f;     /* routed expert FFN width */
+  int32_t S;     /* shared experts (0 allowed) */
+  int32_t f_s;   /* shared expert FFN width */
+  int32_t dtype; /* enum moe_dtype */
+} moe_dims;
+
+/* Human-readable text of a status code (static string). */
+const char* moe_status_string(int status);
+
+/* Bytes of device workspace every call below may use for dims (>= 256). The workspace holds
+ * the device error word, small scratch (per-chunk expert histograms, gate partials) and, for
+ * moe_layer_fwd/bwd, the transient intermediates of the layer. */
+size_t moe_workspace_bytes(const moe_dims* dims);
+
+/* Zero the error word and scratch headers of a fresh workspace (async). Call once after
+ * allocating it. ws: device, >= moe_workspace_bytes(dims) bytes, 256-byte aligned. */
+int moe_workspace_init(void* ws, size_t ws_bytes, const moe_dims* dims, moe_stream_t stream);
+
+/* Synchronise `stream`, copy the workspace error word to *out (MOE_OK if none) and clear it. */
+int moe_get_device_error(void* ws, moe_stream_t stream, int* out);
+
+/* a0. Router scores L = x W_r, fp32 FMA accumulation (no TF32), the router kept in FP32
+ * ("MoE operator optimisation ...", section 4.2).
+ * x [T, d] (dims->dtype), w_r [d][E] fp32 -> logits [T][E] fp32 (written fully). */
+int moe_router_logits(const void* x, const float* w_r, const moe_dims* dims, float* logits,
+                      void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* a1. Fused softmax -> top-k -> renormalised gates -> per-expert counts ("MoE operator
+ * optimisation ...", section 2.1). One warp per token.
+ * logits [T][E] fp32; bias [E] fp32 or NULL (added in fp32 before selection and gating);
+ * -> topk_idx [T][k] int32 (descending score, ties to the lower index), topk_w [T][k] fp32,
+ *    counts [E] int32 (zeroed and filled by this call). Scores must be finite. */
+int moe_route_topk(const float* logits, const float* bias, int64_t T, int32_t E, int32_t k,
+                   int32_t* topk_idx, float* topk_w, int32_t* counts,
+                   void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* a2. VectorSort rearrange (Huawei MoE training-operator article, "VectorSort", Fig. 3):
+ * per-chunk expert histograms -> scan -> stable scatter, all on the device (no host wait,
+ * same article, Fig. 4), with each row moved once in 16-byte vectors.
+ * x [T, d]; topk_idx [T][k]; topk_w [T][k] fp32 or NULL ->
+ *   x_perm [T*k, d] (row dest[q] = x[q / k]), dest [T*k] int32, row_src [T*k] int32,
+ *   offsets [E+1] int32 (exclusive scan of the per-expert counts),
+ *   w_perm [T*k] fp32 or NULL (w_perm[dest[q]] = topk_w[q]).
+ * An id outside [0, E) or repeated within a row records MOE_ERR_DEVICE_EXPERT_ID; such copies
+ * get dest = -1 and are not moved (nothing is written out of bounds). */
+int moe_permute(const void* x, const int32_t* topk_idx, const float* topk_w, const moe_dims* dims,
+                void* x_perm, int32_t* dest, int32_t* row_src, int32_t* offsets, float* w_perm,
+                void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* a2 (gather-only mode, used for dY in the backward): x_perm[dest[q]] = x[q / k] for a dest
+ * from moe_permute. x [T, d] -> x_perm [T*k, d]. Copies with dest < 0 are skipped. */
+int moe_permute_rows(const void* x, const int32_t* dest, const moe_dims* dims, void* x_perm,
+                     moe_stream_t stream);
+
+/* a3. Grouped SwiGLU forward over the ragged expert segments (one persistent tcgen05/TMEM
+ * grouped GEMM launch per matmul for bf16; a SIMT fp32-FMA kernel for fp32); tile schedules
+ * are built on the device from `offsets`.
+ * x_perm [T*k, d], x [T, d] (shared experts' input), w13, w2, ws13, ws2 (NULL if S == 0),
+ * offsets [E+1] ->
+ *   z [T*k, 2f], h [T*k, f] (routed rows), z_sh [S*T, 2f_s], h_sh [S*T, f_s] (shared rows),
+ *   y_perm [T*k, d] (routed expert outputs, ungated), y_sh [T, d] (sum of the shared experts).
+ * Outputs are rounded once to dims->dtype; accumulation is fp32. */
+int moe_grouped_swiglu_fwd(const void* x_perm, const void* x, const void* w13, const void* w2,
+                           const void* ws13, const void* ws2, const int32_t* offsets,
+                           const moe_dims* dims, void* z, void* h, void* z_sh, void* h_sh,
+                           void* y_perm, void* y_sh, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* a4. VectorSort un-rearrange fused with the gate weighting and the shared-expert add
+ * (Huawei MoE training-operator article, Fig. 3; Pangu Ultra MoE article, weighted sum):
+ *   y_t = sum_{j=0..k-1} topk_w[t,j] * y_perm[dest[t*k+j]] + y_sh[t]
+ * summed in fp32 in that order and rounded once. topk_w NULL = weight 1; y_sh may be NULL.
+ * y_perm [T*k, d], dest [T*k] -> y [T, d]. */
+int moe_unpermute_combine(const void* y_perm, const int32_t* dest, const float* topk_w,
+                          const void* y_sh, const moe_dims* dims, void* y, moe_stream_t stream);
+
+/* a5 (expert dX chain; Pangu Ultra MoE article: dW and dX computed separately).
+ *   D = dY_perm W2_e;  dgate_q = sum_f D*h (h recomputed from z);
+ *   dz = [w*D*b*silu'(a) | w*D*silu(a)];  hw = w*h;  dx_perm = dz W13_e.
+ * Shared experts: the same with w = 1 over all T rows, their dX summed into dx_sh.
+ * dy_perm [T*k, d] (moe_permute_rows of dY), dy [T, d], z [T*k, 2f], z_sh [S*T, 2f_s],
+ * w13, w2, ws13, ws2, w_perm [T*k], offsets [E+1], dest [T*k] ->
+ *   dz [T*k, 2f], dz_sh [S*T, 2f_s], hw [T*k, f], hw_sh [S*T, f_s], dx_perm [T*k, d],
+ *   dx_sh [T, d], dgate [T][k] fp32 (token order). */
+int moe_grouped_bwd_dx(const void* dy_perm, const void* dy, const void* z, const void* z_sh,
+                       const void* w13, const void* w2, const void* ws13, const void* ws2,
+                       const float* w_perm, const int32_t* offsets, const int32_t* dest,
+                       const moe_dims* dims, void* dz, void* dz_sh, void* hw, void* hw_sh,
+                       void* dx_perm, void* dx_sh, float* dgate,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* a6 (expert dW products, separate from the dX chain):
+ *   dW2_e = dY_perm_e^T hw_e  ([d][f]),  dW13_e = dz_e^T x_perm_e  ([2f][d]),
+ * reduction over the ragged segment rows; an expert with no rows gets zeros.
+ * Shared: dWs2_s = dY^T hw_sh_s, dWs13_s = dz_sh_s^T x. */
+int moe_grouped_bwd_dw(const void* x_perm, const void* x, const void* hw, const void* hw_sh,
+                       const void* dz, const void* dz_sh, const void* dy_perm, const void* dy,
+                       const int32_t* offsets, const moe_dims* dims,
+                       void* dw13, void* dw2, void* dws13, void* dws2,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Router backward of the renormalised softmax on the top-k:
+ *   dlogits[t, e_j] = w_j (dgate_j - sum_i w_i dgate_i), 0 for experts outside the top-k.
+ * topk_idx, topk_w, dgate [T][k] -> dlogits [T][E] fp32 (written fully). */
+int moe_route_topk_bwd(const int32_t* topk_idx, const float* topk_w, const float* dgate,
+                       int64_t T, int32_t E, int32_t k, float* dlogits, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- whole layer */
+typedef struct moe_layer_params {
+  const float* w_r;  /* [d][E] fp32, or NULL when the caller passes logits_in */
+  const float* bias; /* [E] fp32 constant score bias, or NULL */
+  const void* w13;   /* [E][2f][d] */
+  const void* w2;    /* [E][d][f] */
+  const void* ws13;  /* [S][2f_s][d] or NULL */
+  const void* ws2;   /* [S][d][f_s] or NULL */
+} moe_layer_params;
+
+typedef struct moe_layer_saved { /* caller-allocated; written by moe_layer_fwd, read by _bwd */
+  float* logits;     /* [T][E]: x W_r (without bias); unused when logits_in is given */
+  int32_t* topk_idx; /* [T][k] */
+  float* topk_w;     /* [T][k] */
+  int32_t* counts;   /* [E] */
+  int32_t* offsets;  /* [E+1] */
+  int32_t* dest;     /* [T*k] */
+  int32_t* row_src;  /* [T*k] */
+  float* w_perm;     /* [T*k] */
+  void* x_perm;      /* [T*k, d] */
+  void* z;           /* [T*k, 2f] */
+  void* h;           /* [T*k, f] */
+  void* z_sh;        /* [S*T, 2f_s] or NULL when S == 0 */
+  void* h_sh;        /* [S*T, f_s] or NULL when S == 0 */
+} moe_layer_saved;
+
+typedef struct moe_layer_grads { /* caller-allocated outputs of moe_layer_bwd */
+  void* dx;        /* [T, d]; includes the router term when w_r is given */
+  void* dw13;      /* [E][2f][d] */
+  void* dw2;       /* [E][d][f] */
+  void* dws13;     /* [S][2f_s][d] or NULL when S == 0 */
+  void* dws2;      /* [S][d][f_s] or NULL when S == 0 */
+  float* dw_r;     /* [d][E] fp32, required when w_r is given, else ignored */
+  float* dlogits;  /* [T][E] fp32 gradient w.r.t. the scores; required when logits_in was
+                      given, optional (NULL) otherwise */
+} moe_layer_grads;
+
+/* Forward of one layer: router (unless logits_in), route, permute, grouped SwiGLU,
+ * combine. logits_in [T][E] fp32 or NULL. y [T, d]. No host synchronisation. */
+int moe_layer_fwd(const moe_layer_params* params, const void* x, const float* logits_in,
+                  const moe_dims* dims, const moe_layer_saved* saved, void* y,
+                  void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Backward of one layer from dy [T, d]: permute dY, expert dX chain, dgate -> score
+ * gradient, combine dX (+ router term x-gradient when w_r is given), expert dW products,
+ * router dW_r. The top-k indices are constants (not differentiated); the bias gets no
+ * gradient. `saved` must hold the values moe_layer_fwd wrote for the same x. */
+int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, const void* x,
+                  const void* dy, const moe_dims* dims, const moe_layer_grads* grads,
+                  void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Failure-detection check: runs one bounded wait on a barrier that nothing completes, with
+ * the given limit in nanoseconds, so that it records MOE_ERR_DEVICE_TIMEOUT in the error word
+ * and returns without hanging (read it with moe_get_device_error). */
+int moe_debug_timeout_probe(void* ws, size_t ws_bytes, uint64_t limit_ns, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,120 @@
+"""Helpers shared by the GPU parity tests: run the CUDA layer through the C ABI and the
+fp64 oracle on the same seeded inputs, and compare.
+
+Bars: bit-exact for routing indices, counts, offsets, dest, row_src and the permuted
+rows; ||gpu - oracle|| / ||oracle|| <= 1e-5 for fp32 workloads and for the fp32 gates
+and scores of every workload; <= 5e-3 for bf16 outputs and gradients."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as O
+
+TOL = {"f32": 1e-5, "bf16": 5e-3}
+GATE_TOL = 1e-5
+
+
+def rel(gpu, ref) -> float:
+    a = O.as_f64(gpu)
+    b = np.asarray(ref, np.float64)
+    assert a.shape == b.shape, (a.shape, b.shape)
+    nb = np.linalg.norm(b)
+    na = np.linalg.norm(a - b)
+    if nb == 0.0:
+        return float(na)
+    return float(na / nb)
+
+
+def _to(t, dev="cuda"):
+    return None if t is None else t.to(dev)
+
+
+def run_gpu_layer(w, bwd=True):
+    from dropless_token_routing_gb300.api import LayerParams, MoELayer, get_device_error
+    c = w.cfg
+    params = LayerParams(w13=_to(w.w13), w2=_to(w.w2), w_r=_to(w.w_r), bias=_to(w.bias),
+                         ws13=_to(w.ws13), ws2=_to(w.ws2))
+    layer = MoELayer(params, c["T"], c["d"], c["E"], c["k"], c["f"], c["S"], c["f_s"],
+                     w.torch_dtype, logits_input=w.logits_in is not None)
+    x = _to(w.x)
+    layer.forward(x, _to(w.logits_in))
+    grads = layer.backward(_to(w.dy)) if bwd else None
+    torch.cuda.synchronize()
+    err = get_device_error(layer.ws)
+    return layer, grads, err
+
+
+def oracle_layer(w, device_logits=None, bwd=True):
+    """Oracle forward/backward with the top-k taken on the device's fp32 scores."""
+    k = w.cfg["k"]
+    if w.logits_in is not None:
+        logits32 = w.logits_in.cpu().numpy()
+    else:
+        logits32 = device_logits.detach().cpu().numpy()
+    bias32 = None if w.bias is None else w.bias.cpu().numpy()
+    idx, gate = O.route_topk(O.selection_scores(logits32, bias32), k)
+    x = O.as_f64(w.x)
+    w13, w2, ws13, ws2 = (O.as_f64(t) for t in (w.w13, w.w2, w.ws13, w.ws2))
+    fwd = O.layer_forward(x, idx, gate, w13, w2, ws13, ws2)
+    res = dict(idx=idx, gate=gate, fwd=fwd)
+    if bwd:
+        res["bwd"] = O.layer_backward(x, idx, gate, fwd, O.as_f64(w.dy), w13, w2, ws13, ws2,
+                                      w_r=O.as_f64(w.w_r))
+    return res
+
+
+def check_layer(w, bwd=True, report=None):
+    """Run both sides and assert every bar; returns a dict of the measured errors."""
+    tol = TOL[w.cfg["dtype"]]
+    layer, grads, err = run_gpu_layer(w, bwd=bwd)
+    assert err == 0, f"device error {err}"
+    s = layer.saved
+    errs = {}
+    if w.logits_in is None:
+        ref_logits = O.router_logits(O.as_f64(w.x), O.as_f64(w.w_r))
+        errs["logits"] = rel(s["logits"], ref_logits)
+        assert errs["logits"] <= GATE_TOL, errs
+    ref = oracle_layer(w, device_logits=s["logits"], bwd=bwd)
+    fwd = ref["fwd"]
+    # bit-exact routing and permutation
+    assert np.array_equal(s["topk_idx"].cpu().numpy(), ref["idx"]), "topk_idx differs"
+    assert np.array_equal(s["counts"].cpu().numpy(), fwd["counts"]), "counts differ"
+    assert np.array_equal(s["offsets"].cpu().numpy(), fwd["offsets"]), "offsets differ"
+    assert np.array_equal(s["dest"].cpu().numpy(), fwd["dest"]), "dest differs"
+    assert np.array_equal(s["row_src"].cpu().numpy(), fwd["row_src"]), "row_src differs"
+    assert torch.equal(s["x_perm"].cpu(), w.x[torch.as_tensor(fwd["row_src"])]), "x_perm differs"
+    errs["topk_w"] = rel(s["topk_w"], ref["gate"])
+    errs["w_perm"] = rel(s["w_perm"], fwd["w_perm"])
+    errs["z"] = rel(s["z"], fwd["z"])
+    errs["h"] = rel(s["h"], fwd["h"])
+    errs["y"] = rel(layer.y, fwd["y"])
+    if w.cfg["S"]:
+        errs["z_sh"] = rel(s["z_sh"], np.concatenate(fwd["z_sh"], 0))
+        errs["h_sh"] = rel(s["h_sh"], np.concatenate(fwd["h_sh"], 0))
+    assert errs["topk_w"] <= GATE_TOL and errs["w_perm"] <= GATE_TOL, errs
+    for n in ("z", "h", "y", "z_sh", "h_sh"):
+        if n in errs:
+            assert errs[n] <= tol, (n, errs)
+    if bwd:
+        b = ref["bwd"]
+        errs["dx"] = rel(grads["dx"], b["dx"])
+        errs["dw13"] = rel(grads["dw13"], b["dw13"])
+        errs["dw2"] = rel(grads["dw2"], b["dw2"])
+        if w.cfg["S"]:
+            errs["dws13"] = rel(grads["dws13"], b["dws13"])
+            errs["dws2"] = rel(grads["dws2"], b["dws2"])
+        if grads["dw_r"] is not None:
+            errs["dw_r"] = rel(grads["dw_r"], b["dw_r"])
+        if grads["dlogits"] is not None:
+            errs["dlogits"] = rel(grads["dlogits"], b["dscores"])
+        for n in ("dx", "dw13", "dw2", "dws13", "dws2", "dw_r", "dlogits"):
+            if n in errs:
+                assert errs[n] <= tol, (n, errs)
+        # experts without tokens keep exactly zero gradients
+        empty = np.nonzero(fwd["counts"] == 0)[0]
+        for e in empty:
+            assert not grads["dw13"][int(e)].any() and not grads["dw2"][int(e)].any()
+    if report is not None:
+        report.update(errs)
+    return layer, grads, errs

@@ -1,0 +1,117 @@
+"""The C-ABI library loads, exports every function include/moe.h declares, and its
+host-side argument checks reject bad calls before anything reaches a GPU (CPU only:
+every call here fails validation, so no CUDA API is touched)."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+from dropless_token_routing_gb300 import builder as B
+
+if not os.path.exists(B.LIB):
+    B.build()
+
+from dropless_token_routing_gb300 import _native as N  # noqa: E402
+
+L = N.lib()
+BAD = 0x1008    # not 16-byte aligned; never dereferenced
+GOOD = 0x10000  # aligned fake address, never dereferenced on the paths tested here
+
+
+def dims(**kw):
+    base = dict(T=256, d=512, E=8, k=2, f=256, S=0, f_s=0, dtype=N.MOE_F32)
+    base.update(kw)
+    return N.MoeDims(*[base[n] for n in ("T", "d", "E", "k", "f", "S", "f_s", "dtype")])
+
+
+def test_exports_every_header_function():
+    names = N.header_functions()
+    assert len(names) >= 15
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(L, n)
+
+
+def test_status_strings():
+    for code, name in N.STATUS.items():
+        s = N.status_string(code)
+        assert s and s != "unknown status", name
+    assert N.status_string(12345) == "unknown status"
+
+
+def test_workspace_bytes_and_dims_validation():
+    d = dims()
+    assert L.moe_workspace_bytes(ctypes.byref(d)) > 256
+    assert L.moe_workspace_bytes(ctypes.byref(dims(k=9))) == 0            # k > E
+    assert L.moe_workspace_bytes(ctypes.byref(dims(E=2000, k=2))) == 0    # E > 1024
+    assert L.moe_workspace_bytes(ctypes.byref(dims(dtype=7))) == 0
+    assert L.moe_workspace_bytes(ctypes.byref(dims(d=100))) == 0          # fp32 needs d % 8
+    assert L.moe_workspace_bytes(ctypes.byref(dims(dtype=N.MOE_BF16, d=96))) == 0  # bf16 d % 64
+    assert L.moe_workspace_bytes(ctypes.byref(dims(T=-1))) == 0
+    assert L.moe_workspace_bytes(ctypes.byref(dims(T=0))) >= 256         # T = 0 is valid
+    big = dims(T=16384, d=7680, E=256, k=8, f=2048, S=1, f_s=2048, dtype=N.MOE_BF16)
+    nb = L.moe_workspace_bytes(ctypes.byref(big))
+    assert 4e9 < nb < 2e10
+
+
+def _code(name):
+    return N.STATUS_CODE[name]
+
+
+def test_host_argument_errors():
+    d = dims()
+    ws_n = L.moe_workspace_bytes(ctypes.byref(d))
+    # bad top-k / dims on route_topk
+    assert L.moe_route_topk(GOOD, None, 16, 8, 9, GOOD, GOOD, GOOD, GOOD, 256, None) == _code("MOE_ERR_BAD_TOPK")
+    assert L.moe_route_topk(GOOD, None, 16, 8, 0, GOOD, GOOD, GOOD, GOOD, 256, None) == _code("MOE_ERR_BAD_TOPK")
+    assert L.moe_route_topk(GOOD, None, 16, 0, 1, GOOD, GOOD, GOOD, GOOD, 256, None) == _code("MOE_ERR_BAD_DIMS")
+    assert L.moe_route_topk(None, None, 16, 8, 2, GOOD, GOOD, GOOD, GOOD, 256, None) == _code("MOE_ERR_NULL_POINTER")
+    assert L.moe_route_topk(BAD, None, 16, 8, 2, GOOD, GOOD, GOOD, GOOD, 256, None) == _code("MOE_ERR_MISALIGNED")
+    assert L.moe_route_topk(GOOD, BAD, 16, 8, 2, GOOD, GOOD, GOOD, GOOD, 256, None) == _code("MOE_ERR_MISALIGNED")
+    assert L.moe_route_topk(GOOD, None, 16, 8, 2, GOOD, GOOD, GOOD, GOOD + 16, 256, None) == _code("MOE_ERR_MISALIGNED")
+    assert L.moe_route_topk(GOOD, None, 16, 8, 2, GOOD, GOOD, GOOD, GOOD, 128, None) == _code("MOE_ERR_WORKSPACE_TOO_SMALL")
+    # permute: workspace too small, null output, unsupported dtype
+    assert L.moe_permute(GOOD, GOOD, GOOD, ctypes.byref(d), GOOD, GOOD, GOOD, GOOD, GOOD, GOOD,
+                         ws_n - 1, None) == _code("MOE_ERR_WORKSPACE_TOO_SMALL")
+    assert L.moe_permute(GOOD, GOOD, GOOD, ctypes.byref(d), None, GOOD, GOOD, GOOD, GOOD, GOOD,
+                         ws_n, None) == _code("MOE_ERR_NULL_POINTER")
+    bad_dt = dims(dtype=3)
+    assert L.moe_permute(GOOD, GOOD, GOOD, ctypes.byref(bad_dt), GOOD, GOOD, GOOD, GOOD, GOOD, GOOD,
+                         ws_n, None) == _code("MOE_ERR_UNSUPPORTED_DTYPE")
+    assert L.moe_permute_rows(GOOD, BAD, ctypes.byref(d), GOOD, None) == _code("MOE_ERR_MISALIGNED")
+    # grouped GEMM: shared experts need their buffers
+    ds = dims(S=1, f_s=64)
+    ws_s = L.moe_workspace_bytes(ctypes.byref(ds))
+    assert L.moe_grouped_swiglu_fwd(GOOD, None, GOOD, GOOD, GOOD, GOOD, GOOD, ctypes.byref(ds), GOOD,
+                                    GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, ws_s, None) == _code("MOE_ERR_NULL_POINTER")
+    assert L.moe_unpermute_combine(GOOD, GOOD, BAD, None, ctypes.byref(d), GOOD, None) == _code("MOE_ERR_MISALIGNED")
+    assert L.moe_route_topk_bwd(GOOD, GOOD, GOOD, 4, 8, 9, GOOD, None) == _code("MOE_ERR_BAD_TOPK")
+    # layer calls: router weights or logits must be given; grads need dlogits without W_r
+    p = N.LayerParams(None, None, GOOD, GOOD, None, None)
+    s = N.LayerSaved(*([GOOD] * 13))
+    assert L.moe_layer_fwd(ctypes.byref(p), GOOD, None, ctypes.byref(d), ctypes.byref(s), GOOD, GOOD,
+                           ws_n, None) == _code("MOE_ERR_NULL_POINTER")
+    g = N.LayerGrads(GOOD, GOOD, GOOD, None, None, None, None)
+    assert L.moe_layer_bwd(ctypes.byref(p), ctypes.byref(s), GOOD, GOOD, ctypes.byref(d), ctypes.byref(g),
+                           GOOD, ws_n, None) == _code("MOE_ERR_NULL_POINTER")
+    assert L.moe_layer_fwd(None, GOOD, None, ctypes.byref(d), ctypes.byref(s), GOOD, GOOD, ws_n,
+                           None) == _code("MOE_ERR_NULL_POINTER")
+    assert L.moe_debug_timeout_probe(GOOD + 16, 256, 1000, None) == _code("MOE_ERR_MISALIGNED")
+
+
+def test_import_fails_loudly_without_library(tmp_path, monkeypatch):
+    import importlib
+    import sys
+    monkeypatch.setattr(B, "LIB", str(tmp_path / "missing.so"))
+    sys.modules.pop("dropless_token_routing_gb300._native", None)
+    try:
+        with pytest.raises(ImportError):
+            importlib.import_module("dropless_token_routing_gb300._native")
+    finally:
+        monkeypatch.undo()
+        sys.modules.pop("dropless_token_routing_gb300._native", None)
+        importlib.import_module("dropless_token_routing_gb300._native")

@@ -1,0 +1,155 @@
+"""GPU parity of the individual C-ABI calls against the fp64 oracle, plus the device
+error paths (expert ids out of range, a bounded wait that runs out)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+def _api():
+    from dropless_token_routing_gb300 import api
+    return api
+
+
+def _route(logits, k, bias=None):
+    A = _api()
+    T, E = logits.shape
+    dims = A.make_dims(T, 64, E, k, 64, dtype=torch.float32)
+    ws = A.Workspace(dims)
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    A.route_topk(logits, bias, k, idx, w, counts, ws)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), w.cpu().numpy(), counts.cpu().numpy()
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (24, 3), (64, 6), (256, 8), (1000, 32), (5, 5), (33, 1)])
+def test_route_topk_bitexact_with_ties(E, k):
+    g = torch.Generator().manual_seed(E * 100 + k)
+    T = 777
+    # coarse values: many exact ties, including at the top-k boundary; a few -0.0 / +0.0
+    L = (torch.randint(-6, 7, (T, E), generator=g).float() / 2).contiguous()
+    L[::17, :3] = 0.0
+    L[::19, 1] = -0.0
+    bias = (torch.randint(-2, 3, (E,), generator=g).float() / 4)
+    for b in (None, bias):
+        idx, w, counts = _route(L.cuda(), k, None if b is None else b.cuda())
+        s = O.selection_scores(L.numpy(), None if b is None else b.numpy())
+        ridx, rw = O.route_topk(s, k)
+        assert np.array_equal(idx, ridx)
+        assert np.array_equal(counts, O.expert_counts(ridx, E))
+        assert np.linalg.norm(w - rw) / np.linalg.norm(rw) <= 1e-5
+
+
+def _permute(x, idx, E, w=None):
+    A = _api()
+    T, k = idx.shape
+    d = x.shape[1]
+    dt = x.dtype
+    dims = A.make_dims(T, d, E, k, 64, dtype=dt)
+    ws = A.Workspace(dims)
+    Tk = T * k
+    x_perm = torch.full((Tk, d), 7.0, dtype=dt, device="cuda")
+    dest = torch.empty(Tk, dtype=torch.int32, device="cuda")
+    row_src = torch.full((Tk,), -5, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    w_perm = torch.empty(Tk, dtype=torch.float32, device="cuda") if w is not None else None
+    A.permute(x, idx, w, dims, x_perm, dest, row_src, offsets, w_perm, ws)
+    err = A.get_device_error(ws)
+    return x_perm, dest, row_src, offsets, w_perm, err
+
+
+@pytest.mark.parametrize("T,E,k,skew", [(1, 8, 2, 0), (65, 3, 1, 0), (1000, 24, 3, 0),
+                                         (3000, 256, 8, 1), (130, 7, 7, 0), (4097, 64, 6, 2)])
+def test_permute_matches_stable_counting_sort(T, E, k, skew):
+    g = torch.Generator().manual_seed(T + E)
+    s = torch.randn(T, E, generator=g)
+    if skew == 1:
+        s[:, : E // 4] = -30.0           # dead experts
+        s[: int(0.8 * T), E // 2] = 50.0  # hot expert
+    if skew == 2:
+        s[:, 5] += 3.0
+    idx, _ = O.route_topk(s.numpy(), k)
+    gate = torch.rand(T, k, generator=g)
+    x = torch.randn(T, 64, generator=g).to(torch.bfloat16)
+    x_perm, dest, row_src, offsets, w_perm, err = _permute(
+        x.cuda(), torch.as_tensor(idx, dtype=torch.int32).cuda(), E, gate.cuda())
+    assert err == 0
+    rdest, rsrc = O.permutation(idx, E)
+    assert np.array_equal(dest.cpu().numpy(), rdest)
+    assert np.array_equal(row_src.cpu().numpy(), rsrc)
+    assert np.array_equal(offsets.cpu().numpy(), O.expert_offsets(O.expert_counts(idx, E)))
+    assert torch.equal(x_perm.cpu(), x[torch.as_tensor(rsrc)])
+    wp = np.empty(T * k, np.float32)
+    wp[rdest] = gate.numpy().reshape(-1)
+    assert np.array_equal(w_perm.cpu().numpy(), wp)
+    # gather-only mode and the unweighted / weighted combine
+    A = _api()
+    dims = A.make_dims(T, 64, E, k, 64, dtype=torch.bfloat16)
+    again = torch.zeros_like(x_perm)
+    A.permute_rows(x.cuda(), dest, dims, again)
+    assert torch.equal(again, x_perm)
+    y = torch.empty(T, 64, dtype=torch.bfloat16, device="cuda")
+    A.unpermute_combine(x_perm, dest, None, None, dims, y)
+    ref = O.as_f64(x) * k
+    assert np.allclose(O.as_f64(y), ref, rtol=4e-3, atol=0)
+    A.unpermute_combine(x_perm, dest, torch.as_tensor(gate).cuda(), x.cuda(), dims, y)
+    ref = O.as_f64(x) * (gate.double().sum(1, keepdim=True).numpy() + 1.0)
+    assert np.linalg.norm(O.as_f64(y) - ref) / np.linalg.norm(ref) <= 5e-3
+
+
+def test_permute_rejects_bad_expert_ids_without_writing_out_of_bounds():
+    T, E, k = 200, 8, 2
+    g = torch.Generator().manual_seed(3)
+    idx, _ = O.route_topk(torch.randn(T, E, generator=g).numpy(), k)
+    bad = idx.copy()
+    bad[5, 0] = E          # out of range
+    bad[9, 1] = -1         # negative
+    bad[11, 1] = bad[11, 0]  # repeated within a row
+    x = torch.randn(T, 64, generator=g).to(torch.bfloat16)
+    x_perm, dest, row_src, offsets, _, err = _permute(
+        x.cuda(), torch.as_tensor(bad, dtype=torch.int32).cuda(), E)
+    from dropless_token_routing_gb300._native import STATUS_CODE
+    assert err == STATUS_CODE["MOE_ERR_DEVICE_EXPERT_ID"]
+    d = dest.cpu().numpy()
+    assert d[5 * k + 0] == -1 and d[9 * k + 1] == -1 and d[11 * k + 1] == -1
+    good = d[d >= 0]
+    n_good = T * k - 3
+    assert len(good) == n_good and sorted(good.tolist()) == list(range(n_good))
+    assert offsets[-1].item() == n_good
+    # rows past the valid copies were never written
+    assert torch.all(x_perm[n_good:].float() == 7.0)
+    assert torch.all(row_src[n_good:] == -5)
+
+
+def test_bounded_wait_times_out_with_status():
+    A = _api()
+    from dropless_token_routing_gb300._native import STATUS_CODE
+    dims = A.make_dims(1, 64, 2, 1, 64, dtype=torch.bfloat16)
+    ws = A.Workspace(dims)
+    A.debug_timeout_probe(ws, 2_000_000)  # 2 ms on a barrier nothing completes
+    assert A.get_device_error(ws) == STATUS_CODE["MOE_ERR_DEVICE_TIMEOUT"]
+    assert A.get_device_error(ws) == 0   # reading clears it
+    # the context is still usable afterwards
+    t = torch.ones(1024, device="cuda")
+    assert t.sum().item() == 1024
+
+
+def test_route_topk_bwd_matches_oracle():
+    A = _api()
+    T, E, k = 300, 40, 5
+    g = torch.Generator().manual_seed(11)
+    s = torch.randn(T, E, generator=g)
+    idx, gate = O.route_topk(s.numpy(), k)
+    dgate = torch.randn(T, k, generator=g)
+    out = torch.empty(T, E, device="cuda")
+    A.route_topk_bwd(torch.as_tensor(idx, dtype=torch.int32).cuda(),
+                     torch.as_tensor(gate, dtype=torch.float32).cuda(), dgate.cuda(), E, out)
+    ref = np.zeros((T, E))
+    np.put_along_axis(ref, idx, O.router_backward(gate.astype(np.float32).astype(np.float64),
+                                                  dgate.double().numpy()), axis=1)
+    assert np.linalg.norm(out.cpu().double().numpy() - ref) / np.linalg.norm(ref) <= 1e-5
