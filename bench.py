@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Throughput of the dropless MoE layer (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config pangu_bf16] [--no-cpu-baseline]
+
+One step = the whole hot path over one batch: router scores, fused top-k, permutation,
+grouped SwiGLU forward, combine, and the backward (dY permutation, expert dX chain, score
+gradient, dX combine, expert dW products, router dW), through moe_layer_fwd/moe_layer_bwd.
+The default workload is the Pangu-Ultra-MoE-shaped layer (T=8192, d=7680, 256 routed
+experts, top-8, f=2048, 1 shared expert, Zipf(0.8) routing skew), synthetic and seeded.
+
+N > 1 (torchrun, one process per GPU): every rank runs its own replica of the step
+(weak scaling, no data-path collective); value = tokens processed by all ranks / the
+slowest rank's time.  Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s fwd+bwd"
+UNIT = "tokens/s"
+
+# DRAM traffic per launch from an ncu capture of the dominant kernel, keyed by the phase
+# name; valid only while the kernel source still hashes to src_sha256.
+NCU_TRAFFIC = {}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def _sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()
+
+
+# --------------------------------------------------------------------------- accounting
+def algorithmic_work(cfg):
+    """Per-launch algorithmic FLOPs (tensor phases) or bytes (memory phases) of each phase."""
+    T, d, E, k, f, S, fs = (cfg[n] for n in ("T", "d", "E", "k", "f", "S", "f_s"))
+    es = 4 if cfg["dtype"] == "f32" else 2
+    Tk = T * k
+    rows_f = Tk * f + S * T * fs          # sum over groups of rows x width
+    flops = {
+        "gemm_fwd1": 4.0 * d * rows_f, "gemm_fwd2": 2.0 * d * rows_f,
+        "gemm_bwd2t": 2.0 * d * rows_f, "gemm_bwd1t": 4.0 * d * rows_f,
+        "gemm_dw2": 2.0 * d * rows_f, "gemm_dw13": 4.0 * d * rows_f,
+        "router_gemm": 2.0 * T * d * E,
+    }
+    bytes_ = {
+        "route_topk": 4.0 * T * E + 4.0 * E + 8.0 * Tk,
+        "permute_hist": 4.0 * Tk + 4.0 * Tk + 8.0 * E * ((T + 63) // 64),
+        "permute_scatter": (1 + k) * T * d * es + 24.0 * Tk,
+        "permute_rows": (1 + k) * T * d * es + 4.0 * Tk,
+        "combine": (k + 2 if S else k + 1) * T * d * es + 8.0 * Tk,
+        "combine_bwd": (k + 2 if S else k + 1) * T * d * es + 8.0 * Tk + 8.0 * Tk,
+        "route_bwd": 16.0 * Tk + 4.0 * T * E,
+        "dwr": Tk * d * es + 8.0 * Tk + 4.0 * 8 * E * d,
+    }
+    return flops, bytes_
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.th.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- oracle arm
+def oracle_sample(w, logits32, n_tokens, with_w_r=True):
+    """Time the fp64 oracle's forward + backward on the first n_tokens tokens of a workload
+    (its routing taken from the device's fp32 scores; only the experts those tokens use)."""
+    import numpy as np
+    import oracle as O
+    c = w.cfg
+    rows = slice(0, n_tokens)
+    bias = None if w.bias is None else w.bias.cpu().numpy()
+    idx, gate = O.route_topk(O.selection_scores(logits32[rows], bias), c["k"])
+    used = np.unique(idx)
+    remap = {int(e): i for i, e in enumerate(used)}
+    idx_s = np.vectorize(remap.get)(idx)
+    x = O.as_f64(w.x[rows].cpu())
+    dy = O.as_f64(w.dy[rows].cpu())
+    sel = __import__("torch").as_tensor(used)
+    w13 = O.as_f64(w.w13[sel.to(w.w13.device)].cpu())
+    w2 = O.as_f64(w.w2[sel.to(w.w2.device)].cpu())
+    ws13 = None if w.ws13 is None else O.as_f64(w.ws13.cpu())
+    ws2 = None if w.ws2 is None else O.as_f64(w.ws2.cpu())
+    w_r = O.as_f64(w.w_r[:, sel.to(w.w_r.device)].cpu()) if (with_w_r and w.w_r is not None) else None
+    t0 = time.perf_counter()
+    fwd = O.layer_forward(x, idx_s, gate, w13, w2, ws13, ws2)
+    O.layer_backward(x, idx_s, gate, fwd, dy, w13, w2, ws13, ws2, w_r=w_r)
+    dt = time.perf_counter() - t0
+    return dt, len(used)
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def cpu_baseline(w, logits32, n_tokens):
+    dt, n_exp = oracle_sample(w, logits32, n_tokens)
+    return {"value": n_tokens / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd of the first {n_tokens} tokens of the workload "
+                      f"({n_exp} routed experts they use + shared, full d/f), {dt:.1f} s"}
+
+
+# --------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="pangu_bf16")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-tokens", type=int, default=4)
+    ap.add_argument("--shrink", default="", help="smaller case of the same recipe, e.g. T=512,E=16 "
+                                                  "(for profiler captures; not a bench line)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    from synth import CONFIGS, make_workload, shrink
+    cfg = dict(CONFIGS[args.config], name=args.config)
+    if args.shrink:
+        over = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in args.shrink.split(",")}
+        cfg = shrink(args.config, **over)
+    T = cfg["T"]
+    dtype_name = "bf16" if cfg["dtype"] == "bf16" else "f32"
+    workload_cfg = {"workload": f"{args.config}: T={T} d={cfg['d']} E={cfg['E']} top-{cfg['k']} "
+                                f"f={cfg['f']} S={cfg['S']} f_s={cfg['f_s']} routing={cfg['routing']}"
+                                + (f"(s={cfg['zipf_s']})" if cfg['routing'] == 'zipf' else ""),
+                    "tokens_per_step": T, "l2": "inputs larger than L2 (expert weights > 20 GB)",
+                    "parallelism": f"replicas x{world}"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        w = make_workload(cfg, device=dev)
+        if w.logits_in is not None:
+            logits32 = w.logits_in.cpu().numpy()
+        else:
+            import oracle as O
+            logits32 = O.router_logits(O.as_f64(w.x[:args.oracle_tokens].cpu()),
+                                       O.as_f64(w.w_r.cpu())).astype("float32")
+        for _ in range(args.warmup if False else 0):
+            pass
+        times = []
+        for _ in range(args.steps):
+            dt, n_exp = oracle_sample(w, logits32, args.oracle_tokens)
+            times.append(dt)
+        tot = sum(times)
+        value = args.steps * args.oracle_tokens / tot
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload_cfg,
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                                 "sample": f"each step: fp64 oracle fwd+bwd of the first {args.oracle_tokens} "
+                                           f"tokens ({n_exp} routed experts + shared, full d/f)"},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    from dropless_token_routing_gb300 import _native as N
+    from dropless_token_routing_gb300.api import LayerParams, MoELayer, get_device_error
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = make_workload(cfg, device=dev)
+    params = LayerParams(w13=w.w13, w2=w.w2, w_r=w.w_r, bias=w.bias, ws13=w.ws13, ws2=w.ws2)
+    layer = MoELayer(params, T, cfg["d"], cfg["E"], cfg["k"], cfg["f"], cfg["S"], cfg["f_s"],
+                     w.torch_dtype, device=dev, logits_input=w.logits_in is not None)
+    layer.alloc_grads()
+    x, dy, li = w.x, w.dy, w.logits_in
+    stream = torch.cuda.current_stream()
+
+    def step():
+        layer.forward(x, li)
+        layer.backward(dy)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    err = get_device_error(layer.ws)
+    if err != 0:
+        raise RuntimeError(f"device error {N.STATUS.get(err, err)} during warm-up")
+
+    # ---------------------------------------------------------------- timed region
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    N.trace_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    trace = N.trace_read()
+    N.trace_enable(False)
+    clocks = sampler.stop() if sampler else None
+    t_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([t_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms = float(tt.item())
+    err = get_device_error(layer.ws)
+    if err != 0:
+        raise RuntimeError(f"device error {N.STATUS.get(err, err)} in the timed region")
+    value = world * args.steps * T / (t_ms / 1e3)
+
+    # ---------------------------------------------------------------- end to end
+    h_x = x.cpu().pin_memory()
+    h_dy = dy.cpu().pin_memory()
+    h_li = li.cpu().pin_memory() if li is not None else None
+    h_y = torch.empty_like(h_x).pin_memory()
+    h_dx = torch.empty_like(h_x).pin_memory()
+    d_x, d_dy = torch.empty_like(x), torch.empty_like(dy)
+    d_li = torch.empty_like(li) if li is not None else None
+
+    def e2e_step():
+        d_x.copy_(h_x, non_blocking=True)
+        d_dy.copy_(h_dy, non_blocking=True)
+        if d_li is not None:
+            d_li.copy_(h_li, non_blocking=True)
+        y = layer.forward(d_x, d_li)
+        h_y.copy_(y, non_blocking=True)
+        g = layer.backward(d_dy)
+        h_dx.copy_(g["dx"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k_e2e = max(3, args.steps // 2)
+    e2.record(stream)
+    for _ in range(k_e2e):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = e2.elapsed_time(e3)
+    if world > 1:
+        tt = torch.tensor([t_e2e], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    es = 2 if cfg["dtype"] == "bf16" else 4
+    h2d = 2 * T * cfg["d"] * es + (T * cfg["E"] * 4 if li is not None else 0)
+    d2h = 2 * T * cfg["d"] * es
+    e2e = {"value": world * k_e2e * T / (t_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    # ---------------------------------------------------------------- roofline
+    peaks = _peaks()
+    flops, bytes_ = algorithmic_work(cfg)
+    total_ms = sum(v[1] for v in trace.values())
+    kernels = {}
+    for name, (launches, ms) in sorted(trace.items(), key=lambda kv: -kv[1][1]):
+        per = ms / launches
+        ent = {"launches_per_step": launches / args.steps, "ms_per_launch": round(per, 4),
+               "share": round(ms / total_ms, 4) if total_ms else None}
+        if name in flops and name != "router_gemm":
+            ach = flops[name] / (per / 1e3) / 1e12
+            ent.update(achieved=round(ach, 1), unit="TFLOP/s",
+                       frac=round(ach / peaks["bf16_tflops_sustained"], 3))
+        elif name in bytes_:
+            ach = bytes_[name] / (per / 1e3) / 1e9
+            ent.update(achieved=round(ach, 1), unit="GB/s", frac=round(ach / peaks["hbm_gbs"], 3))
+        elif name == "router_gemm":
+            ent.update(achieved=round(flops[name] / (per / 1e3) / 1e12, 2), unit="TFLOP/s (fp32 FMA)")
+        kernels[name] = ent
+    dom = max(trace.items(), key=lambda kv: kv[1][1])[0]
+    dl, dms = trace[dom]
+    per = dms / dl
+    src = os.path.join(ROOT, "dropless_token_routing_gb300", "csrc", "gemm_tc.cu")
+    traffic = None
+    tr = NCU_TRAFFIC.get(dom)
+    if tr and tr.get("src_sha256") == _sha(src):
+        traffic = tr["bytes_per_launch"]
+    if dom in flops:
+        ach = flops[dom] / (per / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 3), "traffic": traffic, "kernel": dom,
+                "peak_kind": f"bf16 dense, sustained ({peaks['source']})"}
+    else:
+        ach = bytes_[dom] / (per / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 3), "traffic": traffic, "kernel": dom,
+                "peak_kind": f"HBM copy ({peaks['source']})"}
+    gemm_flops = sum(v for k_, v in flops.items() if k_.startswith("gemm"))
+    gemm_ms = sum(trace[k_][1] for k_ in trace if k_.startswith("gemm")) / args.steps
+    launches = sum(v[0] for v in trace.values())
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_ms / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_name,
+            "data": "synthetic (seeded, device-generated)", "config": workload_cfg,
+            "roofline": roof, "gpu_launches": launches, "e2e": e2e, "clocks": clocks,
+            "grouped_gemm": {"tflops": round(gemm_flops / (gemm_ms / 1e3) / 1e12, 1),
+                             "frac_of_dense_peak": round(gemm_flops / (gemm_ms / 1e3) / 1e12 /
+                                                         peaks["bf16_tflops_sustained"], 3)},
+            "kernels": kernels}
+    if not args.no_cpu_baseline and world == 1:
+        logits32 = (li if li is not None else layer.saved["logits"]).cpu().numpy()
+        line["cpu_baseline"] = cpu_baseline(w, logits32, args.oracle_tokens)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

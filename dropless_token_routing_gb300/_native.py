@@ -55,6 +55,10 @@ class LayerSaved(ctypes.Structure):
                 ("h", c_void_p), ("z_sh", c_void_p), ("h_sh", c_void_p)]
 
 
+class TraceEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", c_int64), ("total_ms", ctypes.c_double)]
+
+
 class LayerGrads(ctypes.Structure):
     _fields_ = [("dx", c_void_p), ("dw13", c_void_p), ("dw2", c_void_p), ("dws13", c_void_p),
                 ("dws2", c_void_p), ("dw_r", c_void_p), ("dlogits", c_void_p)]
@@ -83,6 +87,8 @@ _SIGS = {
     "moe_layer_bwd": (c_int, [ctypes.POINTER(LayerParams), ctypes.POINTER(LayerSaved), P, P,
                               ctypes.POINTER(MoeDims), ctypes.POINTER(LayerGrads), P, c_size_t, P]),
     "moe_debug_timeout_probe": (c_int, [P, c_size_t, c_uint64, P]),
+    "moe_trace_enable": (c_int, [c_int]),
+    "moe_trace_read": (c_int, [ctypes.POINTER(TraceEntry), c_int, ctypes.POINTER(c_int)]),
 }
 
 for _name, (_res, _args) in _SIGS.items():
@@ -104,6 +110,18 @@ def lib():
 
 def status_string(s: int) -> str:
     return _lib.moe_status_string(int(s)).decode()
+
+
+def trace_enable(on: bool) -> None:
+    check(_lib.moe_trace_enable(1 if on else 0), "moe_trace_enable")
+
+
+def trace_read() -> dict:
+    """{phase: (launches, total_ms)} of the launches recorded since trace_enable(True)."""
+    buf = (TraceEntry * 64)()
+    n = c_int(0)
+    check(_lib.moe_trace_read(buf, 64, ctypes.byref(n)), "moe_trace_read")
+    return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms)) for i in range(n.value)}
 
 
 def check(status: int, call: str):

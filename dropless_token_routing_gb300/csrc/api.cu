@@ -34,6 +34,7 @@ WsLayout ws_layout(const moe_dims& d) {
   L.dgate = take(4 * Tk);
   L.w_rT = take(4 * E * D);
   L.dwr_part = take(4 * (size_t)kDwrSplit * E * D);
+  L.w_split = take(2 * 3 * E * D);
   L.y_perm = take(es * Tk * D);
   L.y_sh = take(es * T * D);
   L.dy_perm = take(es * Tk * D);
@@ -156,6 +157,20 @@ int zero_expert_grads(const moe_dims* dims, void* dw13, void* dw2, void* dws13, 
   return MOE_OK;
 }
 
+// Router scores: fp32 SIMT FMA for fp32 x; for bf16 x the tensor cores on the exact
+// three-part bf16 split of W_r (products exact, fp32 accumulation).
+int run_router(const void* x, const float* w_r, const moe_dims* d, float* logits, uint8_t* ws,
+               const WsLayout& L, cudaStream_t st) {
+  if (d->dtype == MOE_F32) return launch_router_logits(x, w_r, *d, logits, st) == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+  void* w_split = ws + L.w_split;
+  if (launch_router_split(w_r, d->d, d->E, w_split, st) != cudaSuccess) return MOE_ERR_LAUNCH;
+  GroupedArgs a = base_args(d, nullptr, reinterpret_cast<int*>(ws + L.err));
+  a.x = x;
+  a.w_split = w_split;
+  a.logits_out = logits;
+  return launch_tc_grouped(ROUTER, a, dev_info().sms, st);
+}
+
 int dgate_tiles(const moe_dims* d) {
   return d->dtype == MOE_F32 ? simt_dgate_tiles(d->f) : tc_dgate_tiles(d->f);
 }
@@ -215,9 +230,10 @@ int moe_router_logits(const void* x, const float* w_r, const moe_dims* dims, flo
   MOE_TRY(req(x));
   MOE_TRY(req(w_r));
   MOE_TRY(req(logits));
+  MOE_TRY(check_gemm_device(dims));
   if (dims->T == 0) return MOE_OK;
-  MOE_LAUNCH(launch_router_logits(x, w_r, *dims, logits, (cudaStream_t)stream));
-  return MOE_OK;
+  const WsLayout L = ws_layout(*dims);
+  return run_router(x, w_r, dims, logits, static_cast<uint8_t*>(ws), L, (cudaStream_t)stream);
 }
 
 int moe_route_topk(const float* logits, const float* bias, int64_t T, int32_t E, int32_t k,
@@ -462,7 +478,7 @@ int moe_layer_fwd(const moe_layer_params* params, const void* x, const float* lo
   }
   const float* scores = logits_in;
   if (scores == nullptr) {
-    MOE_LAUNCH(launch_router_logits(x, params->w_r, *dims, saved->logits, st));
+    MOE_TRY(run_router(x, params->w_r, dims, saved->logits, w, L, st));
     scores = saved->logits;
   }
   if (cudaMemsetAsync(saved->counts, 0, sizeof(int32_t) * dims->E, st) != cudaSuccess) return MOE_ERR_CUDA;

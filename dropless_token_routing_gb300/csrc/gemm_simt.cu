@@ -4,6 +4,7 @@
 // memory, the mode's epilogue fused.
 #include "grouped.cuh"
 #include "internal.h"
+#include "trace.h"
 
 namespace moe {
 namespace {
@@ -258,6 +259,8 @@ int simt_dgate_tiles(int f) { return (f + SBN - 1) / SBN; }
 
 cudaError_t launch_simt_grouped(int mode, const GroupedArgs& a, int num_sms, cudaStream_t st) {
   const dim3 grid(2 * num_sms), block(STHREADS);
+  TraceScope ts(mode == FWD1 ? TP_GEMM_FWD1 : mode == FWD2 ? TP_GEMM_FWD2 : mode == BWD2T ? TP_GEMM_BWD2T :
+                mode == BWD1T ? TP_GEMM_BWD1T : mode == DW2 ? TP_GEMM_DW2 : TP_GEMM_DW13, st);
   switch (mode) {
     case FWD1: simt_grouped_kernel<FWD1><<<grid, block, 0, st>>>(a); break;
     case FWD2: simt_grouped_kernel<FWD2><<<grid, block, 0, st>>>(a); break;

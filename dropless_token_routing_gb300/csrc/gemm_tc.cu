@@ -18,6 +18,7 @@
 
 #include "grouped.cuh"
 #include "internal.h"
+#include "trace.h"
 
 namespace moe {
 namespace {
@@ -156,7 +157,10 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
   const int k0 = kb * BK;
   const int row0 = (int)G.row0;
   const int T = (int)a.T;
-  if (MODE == FWD1) {
+  if (MODE == ROUTER) {
+    tma2d(a_s, &p.a0, bar, k0 % a.d, m0);     // x, read once per weight part
+    tma2d(b_s, &p.b0, bar, k0, tc.ni * BN);
+  } else if (MODE == FWD1) {
     const int j0 = tc.ni * (BN / 2);
     if (!G.shared) {
       tma2d(a_s, &p.a0, bar, k0, row0 + m0);
@@ -226,7 +230,27 @@ __device__ __forceinline__ void epilogue_tile(const GroupedArgs& a, const TileCo
   uint32_t u0[32], u1[32];
   float v0[32], v1[32];
 
-  if (MODE == FWD1) {
+  if (MODE == ROUTER) {
+    const int n0 = tc.ni * BN;
+    float* out = a.logits_out + (int64_t)m * a.E;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      if (n0 + c >= G.N) break;
+      tmem_ld32(acc + c, u0);
+      tmem_ld_wait();
+      if (row_ok) {
+        if (n0 + c + 32 <= G.N && (a.E % 4) == 0) {
+          float4* o4 = reinterpret_cast<float4*>(out + n0 + c);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            o4[q] = make_float4(__uint_as_float(u0[4 * q]), __uint_as_float(u0[4 * q + 1]),
+                                __uint_as_float(u0[4 * q + 2]), __uint_as_float(u0[4 * q + 3]));
+        } else {
+          for (int i = 0; i < 32 && n0 + c + i < G.N; ++i) out[n0 + c + i] = __uint_as_float(u0[i]);
+        }
+      }
+    }
+  } else if (MODE == FWD1) {
     const int j0 = tc.ni * (BN / 2);
     __nv_bfloat16 *zr, *hr;
     if (!G.shared) {
@@ -557,6 +581,12 @@ bool map3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr int trace_phase_of(int mode) {
+  return mode == FWD1 ? TP_GEMM_FWD1 : mode == FWD2 ? TP_GEMM_FWD2 : mode == BWD2T ? TP_GEMM_BWD2T
+       : mode == BWD1T ? TP_GEMM_BWD1T : mode == DW2 ? TP_GEMM_DW2 : mode == DW13 ? TP_GEMM_DW13
+       : TP_ROUTER_GEMM;
+}
+
 template <int MODE>
 int launch_mode(TcParams& p, int num_sms, cudaStream_t st) {
   static bool attr_set = false;
@@ -566,6 +596,7 @@ int launch_mode(TcParams& p, int num_sms, cudaStream_t st) {
       return MOE_ERR_CUDA;
     attr_set = true;
   }
+  TraceScope ts(trace_phase_of(MODE), st);
   tc_grouped_kernel<MODE><<<num_sms, NUM_THREADS, SMEM_BYTES, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
 }
@@ -603,6 +634,10 @@ int launch_tc_grouped(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
       if (sh) ok = ok && map2d(&p.a1, g.dz_sh, 2 * fs, ST, 64, 128) && map3d(&p.b1, g.ws13, d, 2 * fs, S, 64, 64);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<BWD1T>(p, num_sms, st);
+    case ROUTER:
+      ok = map2d(&p.a0, g.x, d, T, 64, 128) && map2d(&p.b0, g.w_split, 3 * d, E, 64, 256);
+      if (!ok) return MOE_ERR_CUDA;
+      return launch_mode<ROUTER>(p, num_sms, st);
     case DW2:
       ok = map2d(&p.a0, g.dy_perm, d, Tk, 64, 64) && map2d(&p.b0, g.hw, f, Tk, 64, 64);
       if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 64) && map2d(&p.b1, g.hw_sh, fs, ST, 64, 64);

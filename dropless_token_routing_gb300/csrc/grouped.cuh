@@ -17,7 +17,9 @@ namespace moe {
 //   BWD1T dX = dz W13    [rows, d]   K = 2f       (shared: one group, K = S*2f_s concatenated)
 //   DW2   dW2  = dY^T hw [d, f]      K = rows
 //   DW13  dW13 = dz^T X  [2f, d]     K = rows
-enum Mode : int { FWD1 = 0, FWD2 = 1, BWD2T = 2, BWD1T = 3, DW2 = 4, DW13 = 5 };
+//   ROUTER L  = x Wsplit^T [T, E]     K = 3d       (bf16 x times the three bf16 parts of the
+//                                                   fp32 router weight, fp32 accumulation)
+enum Mode : int { FWD1 = 0, FWD2 = 1, BWD2T = 2, BWD1T = 3, DW2 = 4, DW13 = 5, ROUTER = 6 };
 
 struct GroupedArgs {
   int64_t T, Tk;
@@ -31,12 +33,15 @@ struct GroupedArgs {
   void *z_out, *z_sh_out, *h_out, *h_sh_out, *y_perm, *y_sh;
   void *dz_out, *dz_sh_out, *hw_out, *hw_sh_out, *dx_perm, *dx_sh;
   void *dw13, *dw2, *dws13, *dws2;
+  const void* w_split;      // [E][3d] bf16: hi | mid | lo parts of W_r^T (ROUTER)
+  float* logits_out;        // [T][E] fp32 (ROUTER)
   float* dgate_part;        // [n_tiles_f][Tk] per-N-tile partial sums of dgate (BWD2T)
   int64_t dgate_stride;     // = Tk
   int* err;
 };
 
 __host__ __device__ __forceinline__ int num_groups(int mode, int E, int S) {
+  if (mode == ROUTER) return 1;
   if (mode == FWD2 || mode == BWD1T) return E + (S > 0 ? 1 : 0);
   return E + S;
 }
@@ -52,6 +57,17 @@ struct GroupGeom {
 
 __device__ __forceinline__ GroupGeom group_geom(const GroupedArgs& a, int mode, int g) {
   GroupGeom G;
+  if (mode == ROUTER) {
+    G.shared = false;
+    G.row0 = 0;
+    G.rows = a.T;
+    G.e = 0;
+    G.s = -1;
+    G.M = (int)a.T;
+    G.N = a.E;
+    G.K = 3 * a.d;
+    return G;
+  }
   G.shared = g >= a.E;
   if (!G.shared) {
     const int lo = __ldg(a.offsets + g), hi = __ldg(a.offsets + g + 1);

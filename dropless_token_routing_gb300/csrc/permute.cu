@@ -3,6 +3,7 @@
 // scatter), the row moves in 16-byte vectors, and the gate-weighted combine.
 #include "common.cuh"
 #include "internal.h"
+#include "trace.h"
 
 namespace moe {
 namespace {
@@ -243,14 +244,21 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, const float* topk_
   int32_t* chunk_hist = reinterpret_cast<int32_t*>(ws + L.chunk_hist);
   int32_t* chunk_base = reinterpret_cast<int32_t*>(ws + L.chunk_base);
   int32_t* local_rank = reinterpret_cast<int32_t*>(ws + L.local_rank);
-  permute_hist_kernel<<<(unsigned)L.n_chunks, kChunk, sizeof(uint32_t) * 2 * dm.E, st>>>(
-      idx, dm.T, dm.E, dm.k, L.n_chunks, chunk_hist, local_rank, err);
+  {
+    TraceScope ts(TP_PERMUTE_HIST, st);
+    permute_hist_kernel<<<(unsigned)L.n_chunks, kChunk, sizeof(uint32_t) * 2 * dm.E, st>>>(
+        idx, dm.T, dm.E, dm.k, L.n_chunks, chunk_hist, local_rank, err);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  permute_scan_kernel<<<1, 1024, 0, st>>>(chunk_hist, chunk_base, L.n_chunks, dm.E, offsets);
+  {
+    TraceScope ts(TP_PERMUTE_SCAN, st);
+    permute_scan_kernel<<<1, 1024, 0, st>>>(chunk_hist, chunk_base, L.n_chunks, dm.E, offsets);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const unsigned blocks = (unsigned)token_blocks(dm.T, 8, 1 << 20);
+  TraceScope ts(TP_PERMUTE_SCATTER, st);
   if (dm.dtype == MOE_F32)
     permute_scatter_kernel<float><<<blocks, 256, 0, st>>>(
         (const float*)x, idx, topk_w, local_rank, chunk_base, offsets, dm.T, dm.d, dm.k, L.n_chunks,
@@ -265,6 +273,7 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, const float* topk_
 cudaError_t launch_permute_rows(const void* x, const int32_t* dest, const moe_dims& dm, void* x_perm,
                                 cudaStream_t st) {
   const unsigned blocks = (unsigned)token_blocks(dm.T, 8, 1 << 20);
+  TraceScope ts(TP_PERMUTE_ROWS, st);
   if (dm.dtype == MOE_F32)
     permute_rows_kernel<float><<<blocks, 256, 0, st>>>((const float*)x, dest, dm.T, dm.d, dm.k,
                                                        (float*)x_perm);
@@ -279,6 +288,7 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* dest, const float*
                            const float* w_rT, const moe_dims& dm, void* y, cudaStream_t st) {
   const unsigned blocks = (unsigned)token_blocks(dm.T, 8, 1 << 20);
   const bool router = w_rT != nullptr;
+  TraceScope ts(topk_w != nullptr ? TP_COMBINE : TP_COMBINE_BWD, st);
   if (dm.dtype == MOE_F32) {
     if (router)
       combine_kernel<float, true><<<blocks, 256, 0, st>>>((const float*)y_perm, dest, topk_w,

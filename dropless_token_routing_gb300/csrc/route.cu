@@ -4,6 +4,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "trace.h"
 
 namespace moe {
 namespace {
@@ -183,6 +184,36 @@ __global__ void __launch_bounds__(256) route_bwd_kernel(
   }
 }
 
+// Exact split of the fp32 router weight into three bf16 parts, transposed to K-major:
+// ws[e][j*d + c] = part j of W_r[c][e], with hi = bf16(w), mid = bf16(w - hi),
+// lo = bf16(w - hi - mid).  Each bf16 holds 8 significant bits, every subtraction is exact and
+// the residual shrinks by at least 2^8 per step, so hi + mid + lo == w exactly for every fp32 w
+// of magnitude >= 2^-100 (where the residuals stay normal numbers).
+__global__ void router_split_kernel(const float* __restrict__ w_r, int d, int E,
+                                    __nv_bfloat16* __restrict__ ws) {
+  __shared__ float tile[32][33];
+  const int e0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i, e = e0 + threadIdx.x;
+    tile[i][threadIdx.x] = (c < d && e < E) ? w_r[(int64_t)c * E + e] : 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int e = e0 + i, c = c0 + threadIdx.x;
+    if (e >= E || c >= d) continue;
+    const float v = tile[threadIdx.x][i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    __nv_bfloat16* row = ws + (int64_t)e * 3 * d;
+    row[c] = hi;
+    row[d + c] = mid;
+    row[2 * d + c] = lo;
+  }
+}
+
 // out[c][r] = in[r][c] for an fp32 [rows][cols] matrix.
 __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int cols,
                                      float* __restrict__ out) {
@@ -264,6 +295,7 @@ __global__ void timeout_probe_kernel(int* err, uint64_t limit_ns) {
 cudaError_t launch_router_logits(const void* x, const float* w_r, const moe_dims& dm, float* logits,
                                  cudaStream_t st) {
   const dim3 grid((dm.E + RBN - 1) / RBN, (unsigned)((dm.T + RBM - 1) / RBM)), block(256);
+  TraceScope ts(TP_ROUTER_GEMM, st);
   if (dm.dtype == MOE_F32)
     router_logits_kernel<float><<<grid, block, 0, st>>>((const float*)x, w_r, logits, dm.T, dm.d, dm.E);
   else
@@ -280,6 +312,7 @@ cudaError_t launch_route_topk(const float* logits, const float* bias, int64_t T,
   if (blocks < 1) blocks = 1;
   const size_t sm = sizeof(int) * E;
   const int V = (E + 31) / 32;
+  TraceScope ts(TP_ROUTE_TOPK, st);
 #define MOE_ROUTE_CASE(VV)                                                                   \
   route_topk_kernel<VV><<<(unsigned)blocks, threads, sm, st>>>(logits, bias, T, E, k, idx, w, \
                                                                counts);
@@ -300,14 +333,23 @@ cudaError_t launch_route_bwd(const int32_t* idx, const float* w, const float* dg
   const int threads = 256, wpb = threads / 32;
   int64_t blocks = (T + wpb - 1) / wpb;
   if (blocks > 65535) blocks = 65535;
+  TraceScope ts(TP_ROUTE_BWD, st);
   route_bwd_kernel<<<(unsigned)blocks, threads, 0, st>>>(idx, w, dgate_in, dgate_part, n_part,
                                                          part_stride, dest, T, E, k, dgate_out,
                                                          dlogits, dl_tok, dl_perm);
   return cudaGetLastError();
 }
 
+cudaError_t launch_router_split(const float* w_r, int d, int E, void* w_split, cudaStream_t st) {
+  const dim3 grid((E + 31) / 32, (d + 31) / 32), block(32, 8);
+  TraceScope ts(TP_TRANSPOSE, st);
+  router_split_kernel<<<grid, block, 0, st>>>(w_r, d, E, static_cast<__nv_bfloat16*>(w_split));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_transpose_f32(const float* in, int rows, int cols, float* out, cudaStream_t st) {
   const dim3 grid((cols + 31) / 32, (rows + 31) / 32), block(32, 8);
+  TraceScope ts(TP_TRANSPOSE, st);
   transpose_f32_kernel<<<grid, block, 0, st>>>(in, rows, cols, out);
   return cudaGetLastError();
 }
@@ -316,19 +358,24 @@ cudaError_t launch_dwr(const void* x, const int32_t* row_src, const float* dl_pe
                        const int32_t* offsets, const moe_dims& dm, float* part, float* dw_r,
                        cudaStream_t st) {
   const dim3 g1(dm.E * kDwrSplit, (dm.d + 1023) / 1024), b1(256);
+  {
+  TraceScope ts(TP_DWR, st);
   if (dm.dtype == MOE_F32)
     dwr_partial_kernel<float><<<g1, b1, 0, st>>>((const float*)x, row_src, dl_perm, offsets, dm.d, dm.E, part);
   else
     dwr_partial_kernel<__nv_bfloat16><<<g1, b1, 0, st>>>((const __nv_bfloat16*)x, row_src, dl_perm,
                                                          offsets, dm.d, dm.E, part);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const dim3 g2((dm.d + 31) / 32, (dm.E + 31) / 32), b2(32, 8);
+  TraceScope ts(TP_DWR, st);
   dwr_reduce_kernel<<<g2, b2, 0, st>>>(part, dm.d, dm.E, dw_r);
   return cudaGetLastError();
 }
 
 cudaError_t launch_timeout_probe(int* err, uint64_t limit_ns, cudaStream_t st) {
+  TraceScope ts(TP_MISC, st);
   timeout_probe_kernel<<<1, 32, 0, st>>>(err, limit_ns);
   return cudaGetLastError();
 }

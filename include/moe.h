@@ -228,6 +228,20 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
                   const void* dy, const moe_dims* dims, const moe_layer_grads* grads,
                   void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- tracing */
+/* Per-phase launch timing: while enabled, every kernel launch of the library is bracketed by
+ * a pair of CUDA events on its stream (a few microseconds of host work per launch, no device
+ * synchronisation). moe_trace_enable(1) clears the record and starts; (0) stops and clears.
+ * moe_trace_read waits for the recorded events and fills up to max_entries entries, one per
+ * phase that launched at least once (name is a static string; launches = kernel launches). */
+typedef struct moe_trace_entry {
+  const char* name;
+  int64_t launches;
+  double total_ms;
+} moe_trace_entry;
+int moe_trace_enable(int on);
+int moe_trace_read(moe_trace_entry* out, int max_entries, int* n_out);
+
 /* Failure-detection check: runs one bounded wait on a barrier that nothing completes, with
  * the given limit in nanoseconds, so that it records MOE_ERR_DEVICE_TIMEOUT in the error word
  * and returns without hanging (read it with moe_get_device_error). */

@@ -1,0 +1,204 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py times
+(moe_layer_fwd + moe_layer_bwd on device-generated seeded inputs).
+
+The whole routing and permutation is compared with the oracle (bit-exact).  Float outputs
+are compared on samples the oracle computes one by one: 48 tokens (y, z, h and dx rows,
+score-gradient rows), a handful of experts including the hottest and an empty one (columns
+of dW13 and dW2 over the expert's full segment), and dW_r through the identity
+dW_r = x^T dL, which holds at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import CONFIGS, make_workload
+
+pytestmark = pytest.mark.gpu
+
+SAMPLE_TOKENS = 48
+SAMPLE_COLS = 32
+TOL = 5e-3
+
+
+def _rel(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def _f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+@pytest.fixture(scope="module", params=["mid_bf16", "dsv3_bf16", "pangu_bf16", "adversarial_bf16"])
+def run(request):
+    from dropless_token_routing_gb300.api import LayerParams, MoELayer, get_device_error
+    name = request.param
+    cfg = dict(CONFIGS[name], name=name)
+    w = make_workload(cfg, device="cuda")
+    params = LayerParams(w13=w.w13, w2=w.w2, w_r=w.w_r, bias=w.bias, ws13=w.ws13, ws2=w.ws2)
+    layer = MoELayer(params, cfg["T"], cfg["d"], cfg["E"], cfg["k"], cfg["f"], cfg["S"], cfg["f_s"],
+                     torch.bfloat16, logits_input=w.logits_in is not None)
+    layer.alloc_grads(with_dlogits=True)
+    for _ in range(2):   # run twice: the second pass must not depend on leftovers of the first
+        layer.forward(w.x, w.logits_in)
+        layer.backward(w.dy)
+    torch.cuda.synchronize()
+    assert get_device_error(layer.ws) == 0
+    yield name, cfg, w, layer
+    del layer, w
+    torch.cuda.empty_cache()
+
+
+def _routing(cfg, w, layer):
+    s = layer.saved
+    logits32 = (w.logits_in if w.logits_in is not None else s["logits"]).cpu().numpy()
+    bias32 = None if w.bias is None else w.bias.cpu().numpy()
+    idx, gate = O.route_topk(O.selection_scores(logits32, bias32), cfg["k"])
+    return idx, gate
+
+
+def test_routing_and_permutation_bitexact(run):
+    name, cfg, w, layer = run
+    s = layer.saved
+    idx, gate = _routing(cfg, w, layer)
+    E = cfg["E"]
+    assert np.array_equal(s["topk_idx"].cpu().numpy(), idx)
+    assert _rel(s["topk_w"].cpu().numpy(), gate) <= 1e-5
+    counts = O.expert_counts(idx, E)
+    assert np.array_equal(s["counts"].cpu().numpy(), counts)
+    assert np.array_equal(s["offsets"].cpu().numpy(), O.expert_offsets(counts))
+    dest, row_src = O.permutation(idx, E)
+    assert np.array_equal(s["dest"].cpu().numpy(), dest)
+    assert np.array_equal(s["row_src"].cpu().numpy(), row_src)
+    assert torch.equal(s["x_perm"], w.x[s["row_src"].long()])
+    if name == "adversarial_bf16":
+        info = w.info
+        assert all(counts[e] == 0 for e in info["dead"])
+        assert counts[info["hot"]] == int(np.ceil(0.1 * cfg["T"] * cfg["k"]))
+    if w.logits_in is None:   # device fp32 scores vs fp64 on sampled rows
+        rows = np.linspace(0, cfg["T"] - 1, 64).astype(int)
+        ref = O.router_logits(_f64(w.x[rows]), _f64(w.w_r))
+        assert _rel(s["logits"][rows].cpu().numpy(), ref) <= 1e-5
+
+
+def _sample_tokens(name, cfg, w, idx):
+    T = cfg["T"]
+    g = np.random.default_rng(123)
+    toks = set(g.choice(T, SAMPLE_TOKENS - 8, replace=False).tolist())
+    toks.update([0, T - 1])
+    if name == "adversarial_bf16":
+        toks.update(w.info["boundary_tie_rows"][:3])
+        toks.update(w.info["inner_tie_rows"][:3])
+    return np.array(sorted(toks))
+
+
+def test_sampled_tokens_forward_and_dx(run):
+    name, cfg, w, layer = run
+    idx, gate = _routing(cfg, w, layer)
+    toks = _sample_tokens(name, cfg, w, idx)
+    k, f, d, E, S = cfg["k"], cfg["f"], cfg["d"], cfg["E"], cfg["S"]
+    x = _f64(w.x[toks])
+    dy = _f64(w.dy[toks])
+    y_ref = np.zeros((len(toks), d))
+    dx_ref = np.zeros((len(toks), d))
+    dgate = np.zeros((len(toks), k))
+    z_ref, h_ref = {}, {}
+    dest = layer.saved["dest"].cpu().numpy()
+    for e in np.unique(idx[toks]):
+        W13 = _f64(w.w13[int(e)])
+        W2 = _f64(w.w2[int(e)])
+        for r, t in enumerate(toks):
+            for j in range(k):
+                if idx[t, j] != e:
+                    continue
+                Z, H, Y = O.swiglu_rows(x[r:r + 1], W13, W2)
+                z_ref[t * k + j], h_ref[t * k + j] = Z[0], H[0]
+                y_ref[r] += gate[t, j] * Y[0]
+                D = dy[r:r + 1] @ W2
+                dgate[r, j] = float(np.sum(D * H))
+                a, b = Z[:, :f], Z[:, f:]
+                dz = np.concatenate([gate[t, j] * D * b * O.silu_grad(a), gate[t, j] * D * O.silu(a)], 1)
+                dx_ref[r] += (dz @ W13)[0]
+    for s_ in range(S):
+        W13 = _f64(w.ws13[s_])
+        W2 = _f64(w.ws2[s_])
+        fs = W13.shape[0] // 2
+        Z, H, Y = O.swiglu_rows(x, W13, W2)
+        y_ref += Y
+        D = dy @ W2
+        a, b = Z[:, :fs], Z[:, fs:]
+        dx_ref += np.concatenate([D * b * O.silu_grad(a), D * O.silu(a)], 1) @ W13
+    dl = O.router_backward(gate[toks], dgate)
+    dscores = np.zeros((len(toks), E))
+    np.put_along_axis(dscores, idx[toks], dl, axis=1)
+    if w.w_r is not None:
+        dx_ref += dscores @ _f64(w.w_r).T
+    assert _rel(_f64(layer.y[toks]), y_ref) <= TOL
+    q = np.array(sorted(z_ref))
+    rows = torch.as_tensor(dest[q]).long().cuda()
+    assert _rel(_f64(layer.saved["z"][rows]), np.stack([z_ref[i] for i in q])) <= TOL
+    assert _rel(_f64(layer.saved["h"][rows]), np.stack([h_ref[i] for i in q])) <= TOL
+    g = layer.grads
+    assert _rel(_f64(g["dx"][toks]), dx_ref) <= TOL
+    assert _rel(_f64(g["dlogits"][toks]), dscores) <= TOL
+    # the score gradient of a renormalised softmax sums to zero in every row (all rows)
+    dlg = g["dlogits"].double()
+    assert dlg.sum(1).abs().max().item() <= 1e-5 * max(dlg.abs().max().item(), 1e-30)
+
+
+def _sample_experts(name, cfg, w, counts):
+    E = cfg["E"]
+    order = np.argsort(-counts, kind="stable")
+    ex = [int(order[0]), int(order[len(order) // 2])]
+    empty = np.nonzero(counts == 0)[0]
+    if len(empty):
+        ex.append(int(empty[0]))
+    ex.append(int(np.random.default_rng(7).integers(E)))
+    return sorted(set(ex))
+
+
+def test_sampled_experts_dw(run):
+    name, cfg, w, layer = run
+    idx, gate = _routing(cfg, w, layer)
+    s, g = layer.saved, layer.grads
+    counts = s["counts"].cpu().numpy()
+    offsets = s["offsets"].cpu().numpy()
+    row_src = s["row_src"].cpu().numpy()
+    w_perm = s["w_perm"].cpu().numpy().astype(np.float64)
+    f, d = cfg["f"], cfg["d"]
+    cols = np.random.default_rng(5).choice(f, SAMPLE_COLS, replace=False)
+    for e in _sample_experts(name, cfg, w, counts):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi == lo:
+            assert not g["dw13"][e].any() and not g["dw2"][e].any()
+            continue
+        toks = torch.as_tensor(row_src[lo:hi]).long().cuda()
+        X = _f64(w.x[toks])
+        DY = _f64(w.dy[toks])
+        W13 = _f64(w.w13[e])
+        W2 = _f64(w.w2[e])
+        wr = w_perm[lo:hi, None]
+        A = X @ W13[cols].T                 # gate pre-activations at the sampled columns
+        B = X @ W13[f + cols].T             # up pre-activations
+        D = DY @ W2[:, cols]
+        dza = wr * D * B * O.silu_grad(A)
+        dzb = wr * D * O.silu(A)
+        hw = wr * O.silu(A) * B
+        ref13 = np.concatenate([dza.T @ X, dzb.T @ X], 0)          # rows cols and f+cols
+        got13 = np.concatenate([_f64(g["dw13"][e, cols]), _f64(g["dw13"][e, f + cols])], 0)
+        assert _rel(got13, ref13) <= TOL, e
+        ref2 = DY.T @ hw                                            # dW2[:, cols]
+        assert _rel(_f64(g["dw2"][e][:, cols]), ref2) <= TOL, e
+
+
+def test_router_dw_identity(run):
+    """dW_r = x^T dL with the device's own score gradient (fp64 on the device)."""
+    name, cfg, w, layer = run
+    g = layer.grads
+    if g["dw_r"] is None:
+        pytest.skip("logits are the input of this workload: no router weight")
+    ref = w.x.double().T @ g["dlogits"].double()
+    got = g["dw_r"].double()
+    assert (torch.linalg.norm(got - ref) / torch.linalg.norm(ref)).item() <= 1e-5
