@@ -79,6 +79,23 @@ def algorithmic_work(cfg):
     return flops, bytes_
 
 
+# --------------------------------------------------------------------------- multi-rank
+def reduce_max(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(world: int, steps: int, tokens_per_step: int, t_max_ms: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch (weak scaling)."""
+    return world * steps * tokens_per_step / (t_max_ms / 1e3)
+
+
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
     def __init__(self, gpu_index):
@@ -291,15 +308,11 @@ def main():
     trace = N.trace_read()
     N.trace_enable(False)
     clocks = sampler.stop() if sampler else None
-    t_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([t_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms = float(tt.item())
+    t_ms = reduce_max(e0.elapsed_time(e1), dev)
     err = get_device_error(layer.ws)
     if err != 0:
         raise RuntimeError(f"device error {N.STATUS.get(err, err)} in the timed region")
-    value = world * args.steps * T / (t_ms / 1e3)
+    value = throughput(world, args.steps, T, t_ms)
 
     # ---------------------------------------------------------------- end to end
     h_x = x.cpu().pin_memory()
@@ -332,15 +345,11 @@ def main():
         e2e_step()
     e3.record(stream)
     torch.cuda.synchronize()
-    t_e2e = e2.elapsed_time(e3)
-    if world > 1:
-        tt = torch.tensor([t_e2e], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
+    t_e2e = reduce_max(e2.elapsed_time(e3), dev)
     es = 2 if cfg["dtype"] == "bf16" else 4
     h2d = 2 * T * cfg["d"] * es + (T * cfg["E"] * 4 if li is not None else 0)
     d2h = 2 * T * cfg["d"] * es
-    e2e = {"value": world * k_e2e * T / (t_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    e2e = {"value": throughput(world, k_e2e, T, t_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 
     if rank != 0:

@@ -35,6 +35,7 @@ WsLayout ws_layout(const moe_dims& d) {
   L.w_rT = take(4 * E * D);
   L.dwr_part = take(4 * (size_t)kDwrSplit * E * D);
   L.w_split = take(2 * 3 * E * D);
+  L.router_part = take(4 * (size_t)kRouterSplit * T * ((E + 31) & ~size_t(31)));
   L.y_perm = take(es * Tk * D);
   L.y_sh = take(es * T * D);
   L.dy_perm = take(es * Tk * D);
@@ -79,6 +80,8 @@ int req(const void* p) {
 }
 // optional pointer: may be null; if not, 16-byte aligned
 int opt(const void* p) { return (p == nullptr || aligned16(p)) ? MOE_OK : MOE_ERR_MISALIGNED; }
+// pointer to a buffer whose size is proportional to T: may be null (empty) when T == 0
+int reqT(const void* p, bool t0) { return t0 ? opt(p) : req(p); }
 
 #define MOE_TRY(x)              \
   do {                          \
@@ -167,8 +170,11 @@ int run_router(const void* x, const float* w_r, const moe_dims* d, float* logits
   GroupedArgs a = base_args(d, nullptr, reinterpret_cast<int*>(ws + L.err));
   a.x = x;
   a.w_split = w_split;
-  a.logits_out = logits;
-  return launch_tc_grouped(ROUTER, a, dev_info().sms, st);
+  float* part = reinterpret_cast<float*>(ws + L.router_part);
+  a.logits_out = part;
+  MOE_TRY(launch_tc_grouped(ROUTER, a, dev_info().sms, st));
+  return launch_router_reduce(part, d->T, d->E, kRouterSplit, logits, st) == cudaSuccess ? MOE_OK
+                                                                                        : MOE_ERR_LAUNCH;
 }
 
 int dgate_tiles(const moe_dims* d) {
@@ -226,10 +232,11 @@ int moe_get_device_error(void* ws, moe_stream_t stream, int* out) {
 int moe_router_logits(const void* x, const float* w_r, const moe_dims* dims, float* logits, void* ws,
                       size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_dims(dims));
+  const bool t0 = dims->T == 0;
   MOE_TRY(check_ws(ws, ws_bytes, dims));
-  MOE_TRY(req(x));
+  MOE_TRY(reqT(x, t0));
   MOE_TRY(req(w_r));
-  MOE_TRY(req(logits));
+  MOE_TRY(reqT(logits, t0));
   MOE_TRY(check_gemm_device(dims));
   if (dims->T == 0) return MOE_OK;
   const WsLayout L = ws_layout(*dims);
@@ -244,10 +251,11 @@ int moe_route_topk(const float* logits, const float* bias, int64_t T, int32_t E,
   if (ws == nullptr) return MOE_ERR_NULL_POINTER;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_MISALIGNED;
   if (ws_bytes < 256) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  MOE_TRY(req(logits));
+  const bool t0 = T == 0;
+  MOE_TRY(reqT(logits, t0));
   MOE_TRY(opt(bias));
-  MOE_TRY(req(topk_idx));
-  MOE_TRY(req(topk_w));
+  MOE_TRY(reqT(topk_idx, t0));
+  MOE_TRY(reqT(topk_w, t0));
   MOE_TRY(req(counts));
   const cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -260,15 +268,16 @@ int moe_permute(const void* x, const int32_t* topk_idx, const float* topk_w, con
                 void* x_perm, int32_t* dest, int32_t* row_src, int32_t* offsets, float* w_perm,
                 void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_dims(dims));
+  const bool t0 = dims->T == 0;
   MOE_TRY(check_ws(ws, ws_bytes, dims));
-  MOE_TRY(req(x));
-  MOE_TRY(req(topk_idx));
-  MOE_TRY(req(x_perm));
-  MOE_TRY(req(dest));
-  MOE_TRY(req(row_src));
+  MOE_TRY(reqT(x, t0));
+  MOE_TRY(reqT(topk_idx, t0));
+  MOE_TRY(reqT(x_perm, t0));
+  MOE_TRY(reqT(dest, t0));
+  MOE_TRY(reqT(row_src, t0));
   MOE_TRY(req(offsets));
   MOE_TRY(opt(w_perm));
-  if (w_perm != nullptr) MOE_TRY(req(topk_w));
+  if (w_perm != nullptr) MOE_TRY(reqT(topk_w, t0));
   const cudaStream_t st = (cudaStream_t)stream;
   if (dims->T == 0)
     return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (dims->E + 1), st) == cudaSuccess ? MOE_OK
@@ -283,9 +292,10 @@ int moe_permute(const void* x, const int32_t* topk_idx, const float* topk_w, con
 int moe_permute_rows(const void* x, const int32_t* dest, const moe_dims* dims, void* x_perm,
                      moe_stream_t stream) {
   MOE_TRY(check_dims(dims));
-  MOE_TRY(req(x));
-  MOE_TRY(req(dest));
-  MOE_TRY(req(x_perm));
+  const bool t0 = dims->T == 0;
+  MOE_TRY(reqT(x, t0));
+  MOE_TRY(reqT(dest, t0));
+  MOE_TRY(reqT(x_perm, t0));
   if (dims->T == 0) return MOE_OK;
   MOE_LAUNCH(launch_permute_rows(x, dest, *dims, x_perm, (cudaStream_t)stream));
   return MOE_OK;
@@ -296,21 +306,22 @@ int moe_grouped_swiglu_fwd(const void* x_perm, const void* x, const void* w13, c
                            const moe_dims* dims, void* z, void* h, void* z_sh, void* h_sh,
                            void* y_perm, void* y_sh, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_dims(dims));
+  const bool t0 = dims->T == 0;
   MOE_TRY(check_ws(ws, ws_bytes, dims));
-  MOE_TRY(req(x_perm));
+  MOE_TRY(reqT(x_perm, t0));
   MOE_TRY(req(w13));
   MOE_TRY(req(w2));
   MOE_TRY(req(offsets));
-  MOE_TRY(req(z));
-  MOE_TRY(req(h));
-  MOE_TRY(req(y_perm));
+  MOE_TRY(reqT(z, t0));
+  MOE_TRY(reqT(h, t0));
+  MOE_TRY(reqT(y_perm, t0));
   if (dims->S > 0) {
-    MOE_TRY(req(x));
+    MOE_TRY(reqT(x, t0));
     MOE_TRY(req(ws13));
     MOE_TRY(req(ws2));
-    MOE_TRY(req(z_sh));
-    MOE_TRY(req(h_sh));
-    MOE_TRY(req(y_sh));
+    MOE_TRY(reqT(z_sh, t0));
+    MOE_TRY(reqT(h_sh, t0));
+    MOE_TRY(reqT(y_sh, t0));
   }
   MOE_TRY(check_gemm_device(dims));
   if (dims->T == 0) return MOE_OK;
@@ -328,11 +339,12 @@ int moe_grouped_swiglu_fwd(const void* x_perm, const void* x, const void* w13, c
 int moe_unpermute_combine(const void* y_perm, const int32_t* dest, const float* topk_w,
                           const void* y_sh, const moe_dims* dims, void* y, moe_stream_t stream) {
   MOE_TRY(check_dims(dims));
-  MOE_TRY(req(y_perm));
-  MOE_TRY(req(dest));
+  const bool t0 = dims->T == 0;
+  MOE_TRY(reqT(y_perm, t0));
+  MOE_TRY(reqT(dest, t0));
   MOE_TRY(opt(topk_w));
   MOE_TRY(opt(y_sh));
-  MOE_TRY(req(y));
+  MOE_TRY(reqT(y, t0));
   if (dims->T == 0) return MOE_OK;
   MOE_LAUNCH(launch_combine(y_perm, dest, topk_w, y_sh, nullptr, nullptr, nullptr, *dims, y,
                             (cudaStream_t)stream));
@@ -346,26 +358,27 @@ int moe_grouped_bwd_dx(const void* dy_perm, const void* dy, const void* z, const
                        void* dx_perm, void* dx_sh, float* dgate, void* ws, size_t ws_bytes,
                        moe_stream_t stream) {
   MOE_TRY(check_dims(dims));
+  const bool t0 = dims->T == 0;
   MOE_TRY(check_ws(ws, ws_bytes, dims));
-  MOE_TRY(req(dy_perm));
-  MOE_TRY(req(z));
+  MOE_TRY(reqT(dy_perm, t0));
+  MOE_TRY(reqT(z, t0));
   MOE_TRY(req(w13));
   MOE_TRY(req(w2));
-  MOE_TRY(req(w_perm));
+  MOE_TRY(reqT(w_perm, t0));
   MOE_TRY(req(offsets));
-  MOE_TRY(req(dest));
-  MOE_TRY(req(dz));
-  MOE_TRY(req(hw));
-  MOE_TRY(req(dx_perm));
-  MOE_TRY(req(dgate));
+  MOE_TRY(reqT(dest, t0));
+  MOE_TRY(reqT(dz, t0));
+  MOE_TRY(reqT(hw, t0));
+  MOE_TRY(reqT(dx_perm, t0));
+  MOE_TRY(reqT(dgate, t0));
   if (dims->S > 0) {
-    MOE_TRY(req(dy));
-    MOE_TRY(req(z_sh));
+    MOE_TRY(reqT(dy, t0));
+    MOE_TRY(reqT(z_sh, t0));
     MOE_TRY(req(ws13));
     MOE_TRY(req(ws2));
-    MOE_TRY(req(dz_sh));
-    MOE_TRY(req(hw_sh));
-    MOE_TRY(req(dx_sh));
+    MOE_TRY(reqT(dz_sh, t0));
+    MOE_TRY(reqT(hw_sh, t0));
+    MOE_TRY(reqT(dx_sh, t0));
   }
   MOE_TRY(check_gemm_device(dims));
   if (dims->T == 0) return MOE_OK;
@@ -390,19 +403,20 @@ int moe_grouped_bwd_dw(const void* x_perm, const void* x, const void* hw, const 
                        const int32_t* offsets, const moe_dims* dims, void* dw13, void* dw2,
                        void* dws13, void* dws2, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(check_dims(dims));
+  const bool t0 = dims->T == 0;
   MOE_TRY(check_ws(ws, ws_bytes, dims));
-  MOE_TRY(req(x_perm));
-  MOE_TRY(req(hw));
-  MOE_TRY(req(dz));
-  MOE_TRY(req(dy_perm));
+  MOE_TRY(reqT(x_perm, t0));
+  MOE_TRY(reqT(hw, t0));
+  MOE_TRY(reqT(dz, t0));
+  MOE_TRY(reqT(dy_perm, t0));
   MOE_TRY(req(offsets));
   MOE_TRY(req(dw13));
   MOE_TRY(req(dw2));
   if (dims->S > 0) {
-    MOE_TRY(req(x));
-    MOE_TRY(req(hw_sh));
-    MOE_TRY(req(dz_sh));
-    MOE_TRY(req(dy));
+    MOE_TRY(reqT(x, t0));
+    MOE_TRY(reqT(hw_sh, t0));
+    MOE_TRY(reqT(dz_sh, t0));
+    MOE_TRY(reqT(dy, t0));
     MOE_TRY(req(dws13));
     MOE_TRY(req(dws2));
   }
@@ -424,11 +438,11 @@ int moe_route_topk_bwd(const int32_t* topk_idx, const float* topk_w, const float
                        int32_t E, int32_t k, float* dlogits, moe_stream_t stream) {
   if (E < 1 || E > kMaxE || T < 0) return MOE_ERR_BAD_DIMS;
   if (k < 1 || k > E || k > kMaxK) return MOE_ERR_BAD_TOPK;
+  if (T == 0) return MOE_OK;
   MOE_TRY(req(topk_idx));
   MOE_TRY(req(topk_w));
   MOE_TRY(req(dgate));
   MOE_TRY(req(dlogits));
-  if (T == 0) return MOE_OK;
   MOE_LAUNCH(launch_route_bwd(topk_idx, topk_w, dgate, nullptr, 0, 0, nullptr, T, E, k, nullptr,
                               dlogits, nullptr, nullptr, (cudaStream_t)stream));
   return MOE_OK;
@@ -439,32 +453,33 @@ int moe_layer_fwd(const moe_layer_params* params, const void* x, const float* lo
                   size_t ws_bytes, moe_stream_t stream) {
   if (params == nullptr || saved == nullptr) return MOE_ERR_NULL_POINTER;
   MOE_TRY(check_dims(dims));
+  const bool t0 = dims->T == 0;
   MOE_TRY(check_ws(ws, ws_bytes, dims));
-  MOE_TRY(req(x));
-  MOE_TRY(req(y));
+  MOE_TRY(reqT(x, t0));
+  MOE_TRY(reqT(y, t0));
   MOE_TRY(opt(logits_in));
   MOE_TRY(opt(params->bias));
   if (logits_in == nullptr) {
     MOE_TRY(req(params->w_r));
-    MOE_TRY(req(saved->logits));
+    MOE_TRY(reqT(saved->logits, t0));
   }
-  MOE_TRY(req(saved->topk_idx));
-  MOE_TRY(req(saved->topk_w));
+  MOE_TRY(reqT(saved->topk_idx, t0));
+  MOE_TRY(reqT(saved->topk_w, t0));
   MOE_TRY(req(saved->counts));
   MOE_TRY(req(saved->offsets));
-  MOE_TRY(req(saved->dest));
-  MOE_TRY(req(saved->row_src));
-  MOE_TRY(req(saved->w_perm));
-  MOE_TRY(req(saved->x_perm));
-  MOE_TRY(req(saved->z));
-  MOE_TRY(req(saved->h));
+  MOE_TRY(reqT(saved->dest, t0));
+  MOE_TRY(reqT(saved->row_src, t0));
+  MOE_TRY(reqT(saved->w_perm, t0));
+  MOE_TRY(reqT(saved->x_perm, t0));
+  MOE_TRY(reqT(saved->z, t0));
+  MOE_TRY(reqT(saved->h, t0));
   MOE_TRY(req(params->w13));
   MOE_TRY(req(params->w2));
   if (dims->S > 0) {
     MOE_TRY(req(params->ws13));
     MOE_TRY(req(params->ws2));
-    MOE_TRY(req(saved->z_sh));
-    MOE_TRY(req(saved->h_sh));
+    MOE_TRY(reqT(saved->z_sh, t0));
+    MOE_TRY(reqT(saved->h_sh, t0));
   }
   MOE_TRY(check_gemm_device(dims));
   const cudaStream_t st = (cudaStream_t)stream;
@@ -506,10 +521,11 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
                   size_t ws_bytes, moe_stream_t stream) {
   if (params == nullptr || saved == nullptr || grads == nullptr) return MOE_ERR_NULL_POINTER;
   MOE_TRY(check_dims(dims));
+  const bool t0 = dims->T == 0;
   MOE_TRY(check_ws(ws, ws_bytes, dims));
-  MOE_TRY(req(x));
-  MOE_TRY(req(dy));
-  MOE_TRY(req(grads->dx));
+  MOE_TRY(reqT(x, t0));
+  MOE_TRY(reqT(dy, t0));
+  MOE_TRY(reqT(grads->dx, t0));
   MOE_TRY(req(grads->dw13));
   MOE_TRY(req(grads->dw2));
   MOE_TRY(opt(grads->dlogits));
@@ -518,22 +534,22 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
     MOE_TRY(req(params->w_r));
     MOE_TRY(req(grads->dw_r));
   } else {
-    MOE_TRY(req(grads->dlogits));
+    MOE_TRY(reqT(grads->dlogits, t0));
   }
-  MOE_TRY(req(saved->topk_idx));
-  MOE_TRY(req(saved->topk_w));
+  MOE_TRY(reqT(saved->topk_idx, t0));
+  MOE_TRY(reqT(saved->topk_w, t0));
   MOE_TRY(req(saved->offsets));
-  MOE_TRY(req(saved->dest));
-  MOE_TRY(req(saved->row_src));
-  MOE_TRY(req(saved->w_perm));
-  MOE_TRY(req(saved->x_perm));
-  MOE_TRY(req(saved->z));
+  MOE_TRY(reqT(saved->dest, t0));
+  MOE_TRY(reqT(saved->row_src, t0));
+  MOE_TRY(reqT(saved->w_perm, t0));
+  MOE_TRY(reqT(saved->x_perm, t0));
+  MOE_TRY(reqT(saved->z, t0));
   MOE_TRY(req(params->w13));
   MOE_TRY(req(params->w2));
   if (dims->S > 0) {
     MOE_TRY(req(params->ws13));
     MOE_TRY(req(params->ws2));
-    MOE_TRY(req(saved->z_sh));
+    MOE_TRY(reqT(saved->z_sh, t0));
     MOE_TRY(req(grads->dws13));
     MOE_TRY(req(grads->dws2));
   }

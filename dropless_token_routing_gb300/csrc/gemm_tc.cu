@@ -27,7 +27,7 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * (32 * 144) + 1024;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int kMaxGroups = 1024 + 8;
@@ -107,24 +107,6 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// 32 fp32 -> 32 bf16 (RNE), stored as four 16-byte vectors.
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint4 u;
-    __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q + 0], v[8 * q + 1]);
-    __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q + 2], v[8 * q + 3]);
-    __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q + 4], v[8 * q + 5]);
-    __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q + 6], v[8 * q + 7]);
-    u.x = *reinterpret_cast<uint32_t*>(&h0);
-    u.y = *reinterpret_cast<uint32_t*>(&h1);
-    u.z = *reinterpret_cast<uint32_t*>(&h2);
-    u.w = *reinterpret_cast<uint32_t*>(&h3);
-    d4[q] = u;
-  }
-}
-
 __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v) {
   const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll
@@ -158,8 +140,9 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
   const int row0 = (int)G.row0;
   const int T = (int)a.T;
   if (MODE == ROUTER) {
-    tma2d(a_s, &p.a0, bar, k0 % a.d, m0);     // x, read once per weight part
-    tma2d(b_s, &p.b0, bar, k0, tc.ni * BN);
+    const int kk = G.k0 + k0;                 // K slice of this group
+    tma2d(a_s, &p.a0, bar, kk % a.d, m0);     // x, read once per weight part
+    tma2d(b_s, &p.b0, bar, kk, tc.ni * BN);
   } else if (MODE == FWD1) {
     const int j0 = tc.ni * (BN / 2);
     if (!G.shared) {
@@ -218,37 +201,90 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
 }
 
 // ------------------------------------------------------------------ epilogues
+// Each epilogue warp owns 32 tile rows (its TMEM lane quarter). Results leave in chunks of
+// 128 bytes per row (64 bf16 or 32 fp32 columns): every lane packs its row's chunk into the
+// warp's staging buffer, then the warp re-reads it so that each store instruction writes
+// four whole 128-byte lines. `dst` is this lane's row pointer at the chunk, or null when the
+// row is not stored (ragged M tail).
+constexpr int STAGE_PITCH = 144;                 // 128 B + 16 B pad: conflict-free both ways
+constexpr int WARP_STAGE_BYTES = 32 * STAGE_PITCH;
+
+__device__ __forceinline__ void warp_store_chunk(uint8_t* stage, int lane, const uint4 (&v)[8],
+                                                 void* dst) {
+  uint4* srow = reinterpret_cast<uint4*>(stage + lane * STAGE_PITCH);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) srow[q] = v[q];
+  __syncwarp();
+  const unsigned long long mine = reinterpret_cast<unsigned long long>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = i * 4 + (lane >> 3), q = lane & 7;
+    const unsigned long long ptr = __shfl_sync(0xffffffffu, mine, row);
+    const uint4 val = *reinterpret_cast<const uint4*>(stage + row * STAGE_PITCH + q * 16);
+    if (ptr != 0ull) reinterpret_cast<uint4*>(ptr)[q] = val;
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// 64 fp32 values -> 64 bf16 (RNE) packed in 8 x 16 bytes.
+__device__ __forceinline__ void pack64(const float* f, uint4 (&v)[8]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    v[q] = make_uint4(pack_bf16x2(f[8 * q], f[8 * q + 1]), pack_bf16x2(f[8 * q + 2], f[8 * q + 3]),
+                      pack_bf16x2(f[8 * q + 4], f[8 * q + 5]), pack_bf16x2(f[8 * q + 6], f[8 * q + 7]));
+}
+
+// 64 consecutive fp32 accumulator columns of this lane's row.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* f) {
+  uint32_t a[32], b[32];
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    f[i] = __uint_as_float(a[i]);
+    f[32 + i] = __uint_as_float(b[i]);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ T* row_or_null(bool ok, T* p) { return ok ? p : nullptr; }
+
 // Thread owns tile row r (TMEM lane); `acc` is the TMEM address of its lane, column 0.
 template <int MODE>
 __device__ __forceinline__ void epilogue_tile(const GroupedArgs& a, const TileCoord& tc, int r,
-                                              uint32_t acc) {
+                                              uint32_t acc, uint8_t* stage, int lane) {
   const GroupGeom& G = tc.G;
   const int m0 = tc.mi * BM;
   const int m = m0 + r;
   const bool row_ok = m < G.M;
   const int fw = G.shared ? a.f_s : a.f;
-  uint32_t u0[32], u1[32];
-  float v0[32], v1[32];
+  uint4 pk[8];
 
   if (MODE == ROUTER) {
+    // fp32 partial scores of K slice g, rows padded to a multiple of 32 experts
     const int n0 = tc.ni * BN;
-    float* out = a.logits_out + (int64_t)m * a.E;
+    const int epad = (a.E + 31) & ~31;
+    float* out = a.logits_out + ((int64_t)tc.g * a.T + m) * epad;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 32) {
-      if (n0 + c >= G.N) break;
-      tmem_ld32(acc + c, u0);
-      tmem_ld_wait();
-      if (row_ok) {
-        if (n0 + c + 32 <= G.N && (a.E % 4) == 0) {
-          float4* o4 = reinterpret_cast<float4*>(out + n0 + c);
+      if (n0 + c >= epad) break;
+      uint32_t u[32];
+      if (G.K > 0) {
+        tmem_ld32(acc + c, u);
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            o4[q] = make_float4(__uint_as_float(u0[4 * q]), __uint_as_float(u0[4 * q + 1]),
-                                __uint_as_float(u0[4 * q + 2]), __uint_as_float(u0[4 * q + 3]));
-        } else {
-          for (int i = 0; i < 32 && n0 + c + i < G.N; ++i) out[n0 + c + i] = __uint_as_float(u0[i]);
-        }
+        for (int i = 0; i < 32; ++i) u[i] = 0u;
       }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) pk[q] = make_uint4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
+      warp_store_chunk(stage, lane, pk, row_or_null(row_ok, out + n0 + c));
     }
   } else if (MODE == FWD1) {
     const int j0 = tc.ni * (BN / 2);
@@ -261,23 +297,19 @@ __device__ __forceinline__ void epilogue_tile(const GroupedArgs& a, const TileCo
       hr = (__nv_bfloat16*)a.h_sh_out + ((int64_t)G.s * a.T + m) * a.f_s;
     }
 #pragma unroll 1
-    for (int c = 0; c < BN / 2; c += 32) {
+    for (int c = 0; c < BN / 2; c += 64) {
       if (j0 + c >= fw) break;  // uniform across the warp
-      tmem_ld32(acc + c, u0);
-      tmem_ld32(acc + BN / 2 + c, u1);
-      tmem_ld_wait();
-      if (row_ok) {
+      float g[64], u[64];
+      tmem_ld64(acc + c, g);
+      tmem_ld64(acc + BN / 2 + c, u);
+      pack64(g, pk);
+      warp_store_chunk(stage, lane, pk, row_or_null(row_ok, zr + j0 + c));
+      pack64(u, pk);
+      warp_store_chunk(stage, lane, pk, row_or_null(row_ok, zr + fw + j0 + c));
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v0[i] = __uint_as_float(u0[i]);
-          v1[i] = __uint_as_float(u1[i]);
-        }
-        store_bf16x32(zr + j0 + c, v0);
-        store_bf16x32(zr + fw + j0 + c, v1);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v0[i] = silu_f(v0[i]) * v1[i];
-        store_bf16x32(hr + j0 + c, v0);
-      }
+      for (int i = 0; i < 64; ++i) g[i] = silu_f(g[i]) * u[i];
+      pack64(g, pk);
+      warp_store_chunk(stage, lane, pk, row_or_null(row_ok, hr + j0 + c));
     }
   } else if (MODE == BWD2T) {
     const int n0 = tc.ni * BN;
@@ -296,30 +328,49 @@ __device__ __forceinline__ void epilogue_tile(const GroupedArgs& a, const TileCo
     }
     float dg = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = 0; c < BN; c += 64) {
       if (n0 + c >= fw) break;
-      tmem_ld32(acc + c, u0);
-      tmem_ld_wait();
-      if (row_ok) {
-        float za[32], zb[32];
-        load_bf16x32(zr + n0 + c, za);
-        load_bf16x32(zr + fw + n0 + c, zb);
+      uint4 pa[8], pb[8], ph[8];   // d(gate pre-act), d(up pre-act), gate-weighted h
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float D = __uint_as_float(u0[i]);
-          const float av = za[i], bv = zb[i];
-          const float sg = 1.f / (1.f + expf(-av));
-          const float sl = av * sg;
-          const float hv = sl * bv;
-          dg = fmaf(D, hv, dg);
-          v0[i] = w * D * bv * (sg * (1.f + av * (1.f - sg)));
-          v1[i] = w * D * sl;
-          za[i] = w * hv;
+      for (int half = 0; half < 2; ++half) {
+        const int cc = c + 32 * half;
+        uint32_t u[32];
+        float za[32], zb[32];
+        tmem_ld32(acc + cc, u);
+        tmem_ld_wait();
+        if (row_ok) {
+          load_bf16x32(zr + n0 + cc, za);
+          load_bf16x32(zr + fw + n0 + cc, zb);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) za[i] = zb[i] = 0.f;
         }
-        store_bf16x32(dzr + n0 + c, v0);
-        store_bf16x32(dzr + fw + n0 + c, v1);
-        store_bf16x32(hwr + n0 + c, za);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float va[8], vb[8], vh[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float D = __uint_as_float(u[8 * q + i]);
+            const float av = za[8 * q + i], bv = zb[8 * q + i];
+            const float sg = 1.f / (1.f + expf(-av));
+            const float sl = av * sg;
+            const float hv = sl * bv;
+            dg = fmaf(D, hv, dg);
+            va[i] = w * D * bv * (sg * (1.f + av * (1.f - sg)));
+            vb[i] = w * D * sl;
+            vh[i] = w * hv;
+          }
+          pa[4 * half + q] = make_uint4(pack_bf16x2(va[0], va[1]), pack_bf16x2(va[2], va[3]),
+                                        pack_bf16x2(va[4], va[5]), pack_bf16x2(va[6], va[7]));
+          pb[4 * half + q] = make_uint4(pack_bf16x2(vb[0], vb[1]), pack_bf16x2(vb[2], vb[3]),
+                                        pack_bf16x2(vb[4], vb[5]), pack_bf16x2(vb[6], vb[7]));
+          ph[4 * half + q] = make_uint4(pack_bf16x2(vh[0], vh[1]), pack_bf16x2(vh[2], vh[3]),
+                                        pack_bf16x2(vh[4], vh[5]), pack_bf16x2(vh[6], vh[7]));
+        }
       }
+      warp_store_chunk(stage, lane, pa, row_or_null(row_ok, dzr + n0 + c));
+      warp_store_chunk(stage, lane, pb, row_or_null(row_ok, dzr + fw + n0 + c));
+      warp_store_chunk(stage, lane, ph, row_or_null(row_ok, hwr + n0 + c));
     }
     if (!G.shared && row_ok) a.dgate_part[(int64_t)tc.ni * a.dgate_stride + G.row0 + m] = dg;
   } else {
@@ -345,18 +396,17 @@ __device__ __forceinline__ void epilogue_tile(const GroupedArgs& a, const TileCo
     }
     const bool empty = ModeTraits<MODE>::k_tail && G.K == 0;  // dW of an expert without rows
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = 0; c < BN; c += 64) {
       if (n0 + c >= G.N) break;
+      float v[64];
       if (!empty) {
-        tmem_ld32(acc + c, u0);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(u0[i]);
+        tmem_ld64(acc + c, v);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v0[i] = 0.f;
+        for (int i = 0; i < 64; ++i) v[i] = 0.f;
       }
-      if (row_ok) store_bf16x32(out + n0 + c, v0);
+      pack64(v, pk);
+      warp_store_chunk(stage, lane, pk, row_or_null(row_ok, out + n0 + c));
     }
   }
 }
@@ -509,6 +559,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     // ------------------------------------------------------------ epilogue warps 2..5
     const int lg = warp & 3;              // TMEM lane quarter this warp may access
     const int r = lg * 32 + lane;         // tile row
+    uint8_t* stage = smem + STAGES * STAGE_BYTES + (warp - 2) * WARP_STAGE_BYTES;
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM);
@@ -518,7 +569,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
       if (!__all_sync(0xffffffffu, got)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
       tc_fence_after();
       const uint32_t acc = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(b * BN);
-      epilogue_tile<MODE>(a, tc, r, acc);
+      epilogue_tile<MODE>(a, tc, r, acc, stage, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[b]));

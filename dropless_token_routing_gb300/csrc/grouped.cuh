@@ -18,7 +18,9 @@ namespace moe {
 //   DW2   dW2  = dY^T hw [d, f]      K = rows
 //   DW13  dW13 = dz^T X  [2f, d]     K = rows
 //   ROUTER L  = x Wsplit^T [T, E]     K = 3d       (bf16 x times the three bf16 parts of the
-//                                                   fp32 router weight, fp32 accumulation)
+//                                                   fp32 router weight, fp32 accumulation; the
+//                                                   groups are kRouterSplit K slices whose fp32
+//                                                   partials are summed afterwards in order)
 enum Mode : int { FWD1 = 0, FWD2 = 1, BWD2T = 2, BWD1T = 3, DW2 = 4, DW13 = 5, ROUTER = 6 };
 
 struct GroupedArgs {
@@ -40,8 +42,10 @@ struct GroupedArgs {
   int* err;
 };
 
+constexpr int kRouterSplit = 8;
+
 __host__ __device__ __forceinline__ int num_groups(int mode, int E, int S) {
-  if (mode == ROUTER) return 1;
+  if (mode == ROUTER) return kRouterSplit;
   if (mode == FWD2 || mode == BWD1T) return E + (S > 0 ? 1 : 0);
   return E + S;
 }
@@ -50,6 +54,7 @@ struct GroupGeom {
   int64_t row0;   // first row of the group in the permuted/shared buffers
   int64_t rows;   // rows of the group (token copies)
   int M, N, K;    // matmul shape of the group
+  int k0;         // first K element of the group (ROUTER K slices), else 0
   int e;          // routed expert index, or -1
   int s;          // shared expert index (>= 0 for per-shared-expert groups), or -1
   bool shared;
@@ -65,9 +70,13 @@ __device__ __forceinline__ GroupGeom group_geom(const GroupedArgs& a, int mode, 
     G.s = -1;
     G.M = (int)a.T;
     G.N = a.E;
-    G.K = 3 * a.d;
+    const int nkb = 3 * a.d / 64, per = (nkb + kRouterSplit - 1) / kRouterSplit;
+    const int kb0 = min(g * per, nkb), kb1 = min(kb0 + per, nkb);
+    G.k0 = kb0 * 64;
+    G.K = (kb1 - kb0) * 64;
     return G;
   }
+  G.k0 = 0;
   G.shared = g >= a.E;
   if (!G.shared) {
     const int lo = __ldg(a.offsets + g), hi = __ldg(a.offsets + g + 1);

@@ -32,6 +32,7 @@ struct WsLayout {
   size_t w_rT;         // [E][d] fp32
   size_t dwr_part;     // [kDwrSplit][E][d] fp32
   size_t w_split;      // [E][3d] bf16  exact 3-part split of W_r^T (bf16 router GEMM)
+  size_t router_part;  // [kRouterSplit][T][round32(E)] fp32 K-slice partial scores
   size_t y_perm;       // [T*k, d]  (reused as dx_perm in the backward)
   size_t y_sh;         // [T, d]
   size_t dy_perm;      // [T*k, d]
@@ -65,6 +66,8 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* dest, const float*
                            const void* y_sh, const int32_t* idx, const float* dl_tok,
                            const float* w_rT, const moe_dims& dm, void* y, cudaStream_t st);
 cudaError_t launch_router_split(const float* w_r, int d, int E, void* w_split, cudaStream_t st);
+cudaError_t launch_router_reduce(const float* part, int64_t T, int E, int nsplit, float* logits,
+                                 cudaStream_t st);
 cudaError_t launch_transpose_f32(const float* in, int rows, int cols, float* out, cudaStream_t st);
 cudaError_t launch_dwr(const void* x, const int32_t* row_src, const float* dl_perm,
                        const int32_t* offsets, const moe_dims& dm, float* part, float* dw_r,

@@ -214,6 +214,21 @@ __global__ void router_split_kernel(const float* __restrict__ w_r, int d, int E,
   }
 }
 
+// logits[t][e] = sum over the K slices g (in order) of part[g][t][e]; part rows are padded
+// to a multiple of 32 experts.
+__global__ void router_reduce_kernel(const float* __restrict__ part, int64_t T, int E, int epad,
+                                     int nsplit, float* __restrict__ logits) {
+  const int64_t n = T * E;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / E;
+    const int e = (int)(i - t * E);
+    float s = 0.f;
+    for (int g = 0; g < nsplit; ++g) s += part[((int64_t)g * T + t) * epad + e];
+    logits[i] = s;
+  }
+}
+
 // out[c][r] = in[r][c] for an fp32 [rows][cols] matrix.
 __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int cols,
                                      float* __restrict__ out) {
@@ -344,6 +359,15 @@ cudaError_t launch_router_split(const float* w_r, int d, int E, void* w_split, c
   const dim3 grid((E + 31) / 32, (d + 31) / 32), block(32, 8);
   TraceScope ts(TP_TRANSPOSE, st);
   router_split_kernel<<<grid, block, 0, st>>>(w_r, d, E, static_cast<__nv_bfloat16*>(w_split));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_reduce(const float* part, int64_t T, int E, int nsplit, float* logits,
+                                 cudaStream_t st) {
+  int64_t blocks = (T * E + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  TraceScope ts(TP_ROUTER_GEMM, st);
+  router_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(part, T, E, (E + 31) & ~31, nsplit, logits);
   return cudaGetLastError();
 }
 
