@@ -400,6 +400,11 @@ def main():
     gemm_ms = sum(trace[k_][1] for k_ in trace if k_.startswith("gemm")) / args.steps
     launches = sum(v[0] for v in trace.values())
 
+    cnt = layer.saved["counts"].cpu().tolist()
+    rows = sum(cnt) + cfg["S"] * T
+    padded = sum(-(-c // 128) * 128 for c in cnt) + cfg["S"] * (-(-T // 128) * 128)
+    routing_stats = {"max_expert_rows": max(cnt), "empty_experts": sum(1 for c in cnt if c == 0),
+                     "m_tile_fill": round(rows / padded, 4)}
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_ms / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_name,
@@ -408,7 +413,7 @@ def main():
             "grouped_gemm": {"tflops": round(gemm_flops / (gemm_ms / 1e3) / 1e12, 1),
                              "frac_of_dense_peak": round(gemm_flops / (gemm_ms / 1e3) / 1e12 /
                                                          peaks["bf16_tflops_sustained"], 3)},
-            "kernels": kernels}
+            "routing": routing_stats, "kernels": kernels}
     if not args.no_cpu_baseline and world == 1:
         logits32 = (li if li is not None else layer.saved["logits"]).cpu().numpy()
         line["cpu_baseline"] = cpu_baseline(w, logits32, args.oracle_tokens)

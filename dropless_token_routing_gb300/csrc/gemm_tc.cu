@@ -5,13 +5,15 @@
 //   warp 1      TMEM owner and single-thread tcgen05.mma issuer (M=128, N=256, K=16 steps,
 //               fp32 accumulators in TMEM, two accumulator buffers of 256 columns)
 //   warps 2..5  epilogue: tcgen05.ld -> fused math of the mode -> bf16 -> global memory
+//   warp 6      (dW products only) ragged-K fix-up: zeroes the A rows past an expert's
+//               segment in the last K block of a tile, so the producer never blocks on it
 // The tile schedule (groups = routed experts with ragged row counts, then shared experts)
 // is rebuilt by every CTA from the device-resident expert offsets, so nothing waits on the
 // host. Tiles of one expert run N-tile major / M-tile minor so concurrently running CTAs
 // share the expert's weight tile through L2.
 // Ragged edges: M tails read neighbouring rows (or the TMA zero fill) and are not stored;
 // ragged K (the dW products reduce over an expert's rows) zeroes the out-of-segment rows of
-// the A tile in shared memory before the last MMA of the tile.
+// the A tile in shared memory (warp 6) before the last MMA of the tile.
 // Every mbarrier wait is bounded (1 s); on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT,
 // drains its TMA loads and MMAs, frees its TMEM and exits.
 #include <cuda.h>
@@ -27,14 +29,16 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * (32 * 144) + 1024;
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_STAGE_BYTES = 5120;        // per epilogue warp, a multiple of 1024
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_STAGE_BYTES + 1024;
+constexpr int NUM_THREADS = 224;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int kMaxGroups = 1024 + 8;
 constexpr int SLAB = 64 * 128;                // one 64-element-wide, 64-row swizzled slab
 
 struct TcParams {
   CUtensorMap a0, a1, b0, b1;
+  CUtensorMap o0, o1;  // output maps of the dW products (routed / shared), box {64, 32, 1}
   GroupedArgs g;
 };
 
@@ -56,6 +60,18 @@ __device__ __forceinline__ void tma3d(uint32_t dst, const CUtensorMap* map, uint
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+
+__device__ __forceinline__ void tma_store3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -207,7 +223,7 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
 // four whole 128-byte lines. `dst` is this lane's row pointer at the chunk, or null when the
 // row is not stored (ragged M tail).
 constexpr int STAGE_PITCH = 144;                 // 128 B + 16 B pad: conflict-free both ways
-constexpr int WARP_STAGE_BYTES = 32 * STAGE_PITCH;
+static_assert(32 * STAGE_PITCH <= EPI_STAGE_BYTES, "staging buffer too small");
 
 __device__ __forceinline__ void warp_store_chunk(uint8_t* stage, int lane, const uint4 (&v)[8],
                                                  void* dst) {
@@ -257,8 +273,9 @@ __device__ __forceinline__ T* row_or_null(bool ok, T* p) { return ok ? p : nullp
 
 // Thread owns tile row r (TMEM lane); `acc` is the TMEM address of its lane, column 0.
 template <int MODE>
-__device__ __forceinline__ void epilogue_tile(const GroupedArgs& a, const TileCoord& tc, int r,
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileCoord& tc, int r,
                                               uint32_t acc, uint8_t* stage, int lane) {
+  const GroupedArgs& a = p.g;
   const GroupGeom& G = tc.G;
   const int m0 = tc.mi * BM;
   const int m = m0 + r;
@@ -373,38 +390,53 @@ __device__ __forceinline__ void epilogue_tile(const GroupedArgs& a, const TileCo
       warp_store_chunk(stage, lane, ph, row_or_null(row_ok, hwr + n0 + c));
     }
     if (!G.shared && row_ok) a.dgate_part[(int64_t)tc.ni * a.dgate_stride + G.row0 + m] = dg;
-  } else {
+  } else if (MODE == DW2 || MODE == DW13) {
+    // dW tiles have no ragged rows: each warp stages its 32 x 64 chunk in the 128-byte
+    // swizzled layout and one lane hands it to the TMA engine (asynchronous tensor store).
+    const int n0 = tc.ni * BN;
+    const int rowc = m0 + (r - lane);          // first row of this warp's 32
+    const CUtensorMap* om = G.shared ? &p.o1 : &p.o0;
+    const int zc = G.shared ? G.s : G.e;
+    const bool empty = G.K == 0;               // dW of an expert without rows
+    if (rowc < G.M) {
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 64) {
+        if (n0 + c >= G.N) break;
+        float v[64];
+        if (!empty) {
+          tmem_ld64(acc + c, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) v[i] = 0.f;
+        }
+        pack64(v, pk);
+        if (lane == 0) bulk_wait_read0();      // the previous store has left the buffer
+        __syncwarp();
+        uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) srow[q ^ (lane & 7)] = pk[q];
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          tma_store3d(om, smem_u32(stage), n0 + c, rowc, zc);
+          bulk_commit();
+        }
+      }
+    }
+  } else {  // FWD2 / BWD1T: rows of ragged expert segments, stored row by row
     const int n0 = tc.ni * BN;
     __nv_bfloat16* out;
-    switch (MODE) {
-      case FWD2:
-        out = G.shared ? (__nv_bfloat16*)a.y_sh + (int64_t)m * a.d
-                       : (__nv_bfloat16*)a.y_perm + (G.row0 + m) * (int64_t)a.d;
-        break;
-      case BWD1T:
-        out = G.shared ? (__nv_bfloat16*)a.dx_sh + (int64_t)m * a.d
-                       : (__nv_bfloat16*)a.dx_perm + (G.row0 + m) * (int64_t)a.d;
-        break;
-      case DW2:
-        out = G.shared ? (__nv_bfloat16*)a.dws2 + ((int64_t)G.s * a.d + m) * a.f_s
-                       : (__nv_bfloat16*)a.dw2 + ((int64_t)G.e * a.d + m) * a.f;
-        break;
-      default:  // DW13
-        out = G.shared ? (__nv_bfloat16*)a.dws13 + ((int64_t)G.s * 2 * a.f_s + m) * a.d
-                       : (__nv_bfloat16*)a.dw13 + ((int64_t)G.e * 2 * a.f + m) * a.d;
-        break;
-    }
-    const bool empty = ModeTraits<MODE>::k_tail && G.K == 0;  // dW of an expert without rows
+    if (MODE == FWD2)
+      out = G.shared ? (__nv_bfloat16*)a.y_sh + (int64_t)m * a.d
+                     : (__nv_bfloat16*)a.y_perm + (G.row0 + m) * (int64_t)a.d;
+    else
+      out = G.shared ? (__nv_bfloat16*)a.dx_sh + (int64_t)m * a.d
+                     : (__nv_bfloat16*)a.dx_perm + (G.row0 + m) * (int64_t)a.d;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 64) {
       if (n0 + c >= G.N) break;
       float v[64];
-      if (!empty) {
-        tmem_ld64(acc + c, v);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] = 0.f;
-      }
+      tmem_ld64(acc + c, v);
       pack64(v, pk);
       warp_store_chunk(stage, lane, pk, row_or_null(row_ok, out + n0 + c));
     }
@@ -417,11 +449,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
   using TR = ModeTraits<MODE>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
-  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], tail_bar, final_bar;
+  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], tail_bar[STAGES], final_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
   __shared__ int tile_start[kMaxGroups + 1];
   __shared__ int warp_sums[32];
+  __shared__ int s_off[1024 + 1];
 
   const GroupedArgs& a = p.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -438,7 +471,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
       mbar_init(smem_u32(&tfull_bar[b]), 1);
       mbar_init(smem_u32(&tempty_bar[b]), 4);
     }
-    mbar_init(smem_u32(&tail_bar), 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&tail_bar[s]), 1);
     mbar_init(smem_u32(&final_bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -451,7 +484,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     tc_fence_before();
   }
-  build_tile_starts(a, MODE, BM, TR::bn_eff, tile_start, warp_sums);  // ends with __syncthreads
+  build_tile_starts(a, MODE, BM, TR::bn_eff, tile_start, warp_sums, s_off);  // ends with __syncthreads
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
   const int ng = num_groups(MODE, a.E, a.S);
@@ -460,60 +493,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     int stage = 0;
-    uint32_t phase = 0, tail_phase = 0;
-    uint32_t pending = 0;            // stages whose latest load may still be in flight
-    uint32_t pend_par = 0;           // parity of that load's phase, per stage
-    bool tail_pending = false;
+    uint32_t phase = 0;
+    uint32_t pending = 0;    // stages whose latest load may still be in flight
+    uint32_t pend_par = 0;   // parity of the phase that load completes, per stage
+    uint32_t pend_tail = 0;  // ... and whether it completes on tail_bar (else full_bar)
+    uint32_t tail_par = 0;   // next tail_bar parity, per stage
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM);
+      const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM, s_off);
       const int nkb = (tc.G.K + BK - 1) / BK;
       for (int kb = 0; kb < nkb; ++kb) {
         const bool got = mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, &abort_flag,
                                            a.err, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
-        const int rem = tc.G.K - kb * BK;
-        const bool tail = TR::k_tail && rem < BK;
-        const uint32_t fb = smem_u32(&full_bar[stage]);
-        if (!tail) {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, fb);
-          }
-          pending |= 1u << stage;
-          pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-        } else {
-          const uint32_t tb = smem_u32(&tail_bar);
-          if (lane == 0) {
-            mbar_arrive_expect_tx(tb, STAGE_BYTES);
-            issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, tb);
-          }
-          tail_pending = true;
-          const bool landed = mbar_wait_bounded(tb, tail_phase, &abort_flag, a.err, kWaitLimitNs);
-          if (!__all_sync(0xffffffffu, landed)) { ok = false; break; }
-          tail_pending = false;
-          tail_phase ^= 1u;
-          // zero K rows [rem, 64) of both 64-wide slabs of the MN-major A tile
-          uint4* A4 = reinterpret_cast<uint4*>(smem + stage * STAGE_BYTES);
-          const int per_slab = (BK - rem) * 8;  // 16-byte chunks
-          for (int i = lane; i < 2 * per_slab; i += 32) {
-            const int sl = i / per_slab, j = i - sl * per_slab;
-            A4[sl * (SLAB / 16) + rem * 8 + j] = make_uint4(0u, 0u, 0u, 0u);
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(fb);
-          pending &= ~(1u << stage);
+        const bool tail = TR::k_tail && tc.G.K - kb * BK < BK;
+        // a ragged last K block lands on tail_bar; warp 6 zeroes it and then completes full_bar
+        const uint32_t bar = tail ? smem_u32(&tail_bar[stage]) : smem_u32(&full_bar[stage]);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, STAGE_BYTES);
+          issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, bar);
         }
+        const uint32_t par = tail ? (tail_par >> stage) & 1u : phase;
+        pending |= 1u << stage;
+        pend_par = (pend_par & ~(1u << stage)) | (par << stage);
+        pend_tail = (pend_tail & ~(1u << stage)) | ((tail ? 1u : 0u) << stage);
+        if (tail) tail_par ^= 1u << stage;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
     // drain: no TMA load may still be writing shared memory when the CTA exits
     for (int s = 0; s < STAGES; ++s)
       if ((pending >> s) & 1u)
-        mbar_wait_bounded(smem_u32(&full_bar[s]), (pend_par >> s) & 1u, nullptr, a.err, kWaitLimitNs);
-    if (tail_pending) mbar_wait_bounded(smem_u32(&tail_bar), tail_phase, nullptr, a.err, kWaitLimitNs);
+        mbar_wait_bounded(smem_u32((pend_tail >> s) & 1u ? &tail_bar[s] : &full_bar[s]),
+                          (pend_par >> s) & 1u, nullptr, a.err, kWaitLimitNs);
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ ragged-K fix-up (dW only)
+    if (TR::k_tail) {
+      int stage = 0;
+      uint32_t tail_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM, s_off);
+        const int nkb = (tc.G.K + BK - 1) / BK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int rem = tc.G.K - kb * BK;
+          if (rem < BK) {
+            const bool got = mbar_wait_bounded(smem_u32(&tail_bar[stage]), (tail_par >> stage) & 1u,
+                                               &abort_flag, a.err, kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+            tail_par ^= 1u << stage;
+            // zero K rows [rem, roundup16(rem)) of both 64-wide slabs of the MN-major A tile;
+            // the MMA issuer stops at roundup16(rem), so rows past that are never read
+            uint4* A4 = reinterpret_cast<uint4*>(smem + stage * STAGE_BYTES);
+            const int per_slab = (((rem + 15) & ~15) - rem) * 8;  // 16-byte chunks
+            for (int i = lane; i < 2 * per_slab; i += 32) {
+              const int sl = i / per_slab, j = i - sl * per_slab;
+              A4[sl * (SLAB / 16) + rem * 8 + j] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&full_bar[stage]));
+          }
+          if (++stage == STAGES) stage = 0;
+        }
+      }
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (one thread)
     if (lane == 0) {
@@ -523,7 +568,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
       bool issued = false, ok = true;
       int it = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-        const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM);
+        const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM, s_off);
         const int nkb = (tc.G.K + BK - 1) / BK;
         const int b = it & 1;
         if (!mbar_wait_bounded(smem_u32(&tempty_bar[b]), ((it >> 1) & 1) ^ 1, &abort_flag, a.err,
@@ -535,8 +580,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
                                  kWaitLimitNs)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
+          // K=16 steps in this block: 4, or fewer in a ragged last block of a dW product
+          const int nks = TR::k_tail ? min(BK, tc.G.K - kb * BK + 15) / 16 : BK / 16;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
+            if (kk >= nks) break;
             const uint64_t ad = TR::a_mn ? sdesc(a_s + kk * 2048, SLAB, 1024) : sdesc(a_s + kk * 32, 16, 1024);
             const uint64_t bd = TR::b_mn ? sdesc(b_s + kk * 2048, SLAB, 1024) : sdesc(b_s + kk * 32, 16, 1024);
             umma(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
@@ -555,25 +603,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ epilogue warps 2..5
     const int lg = warp & 3;              // TMEM lane quarter this warp may access
     const int r = lg * 32 + lane;         // tile row
-    uint8_t* stage = smem + STAGES * STAGE_BYTES + (warp - 2) * WARP_STAGE_BYTES;
+    uint8_t* stage = smem + STAGES * STAGE_BYTES + (warp - 2) * EPI_STAGE_BYTES;
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM);
+      const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM, s_off);
       const int b = it & 1;
       const bool got = mbar_wait_bounded(smem_u32(&tfull_bar[b]), (it >> 1) & 1, &abort_flag,
                                          a.err, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, got)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
       tc_fence_after();
       const uint32_t acc = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(b * BN);
-      epilogue_tile<MODE>(a, tc, r, acc, stage, lane);
+      epilogue_tile<MODE>(p, tc, r, acc, stage, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[b]));
     }
+    if (lane == 0) bulk_wait0();  // tensor stores of the dW products fully written
   }
   __syncthreads();
   if (warp == 1) {
@@ -690,13 +739,17 @@ int launch_tc_grouped(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<ROUTER>(p, num_sms, st);
     case DW2:
-      ok = map2d(&p.a0, g.dy_perm, d, Tk, 64, 64) && map2d(&p.b0, g.hw, f, Tk, 64, 64);
-      if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 64) && map2d(&p.b1, g.hw_sh, fs, ST, 64, 64);
+      ok = map2d(&p.a0, g.dy_perm, d, Tk, 64, 64) && map2d(&p.b0, g.hw, f, Tk, 64, 64) &&
+           map3d(&p.o0, g.dw2, f, d, E, 64, 32);
+      if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 64) && map2d(&p.b1, g.hw_sh, fs, ST, 64, 64) &&
+                   map3d(&p.o1, g.dws2, fs, d, S, 64, 32);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<DW2>(p, num_sms, st);
     default:
-      ok = map2d(&p.a0, g.dz, 2 * f, Tk, 64, 64) && map2d(&p.b0, g.x_perm, d, Tk, 64, 64);
-      if (sh) ok = ok && map2d(&p.a1, g.dz_sh, 2 * fs, ST, 64, 64) && map2d(&p.b1, g.x, d, T, 64, 64);
+      ok = map2d(&p.a0, g.dz, 2 * f, Tk, 64, 64) && map2d(&p.b0, g.x_perm, d, Tk, 64, 64) &&
+           map3d(&p.o0, g.dw13, d, 2 * f, E, 64, 32);
+      if (sh) ok = ok && map2d(&p.a1, g.dz_sh, 2 * fs, ST, 64, 64) && map2d(&p.b1, g.x, d, T, 64, 64) &&
+                   map3d(&p.o1, g.dws13, d, 2 * fs, S, 64, 32);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<DW13>(p, num_sms, st);
   }

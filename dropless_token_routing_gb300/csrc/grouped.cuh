@@ -60,7 +60,8 @@ struct GroupGeom {
   bool shared;
 };
 
-__device__ __forceinline__ GroupGeom group_geom(const GroupedArgs& a, int mode, int g) {
+// `offs` is the expert offsets array [E+1] (a shared-memory copy inside the kernels).
+__device__ __forceinline__ GroupGeom group_geom(const GroupedArgs& a, int mode, int g, const int* offs) {
   GroupGeom G;
   if (mode == ROUTER) {
     G.shared = false;
@@ -79,7 +80,7 @@ __device__ __forceinline__ GroupGeom group_geom(const GroupedArgs& a, int mode, 
   G.k0 = 0;
   G.shared = g >= a.E;
   if (!G.shared) {
-    const int lo = __ldg(a.offsets + g), hi = __ldg(a.offsets + g + 1);
+    const int lo = offs[g], hi = offs[g + 1];
     G.row0 = lo;
     G.rows = hi - lo;
     G.e = g;
@@ -103,11 +104,16 @@ __device__ __forceinline__ GroupGeom group_geom(const GroupedArgs& a, int mode, 
   return G;
 }
 
-// Block-wide exclusive scan of per-group tile counts into tile_start[0..ng] (shared memory).
-// Every thread of the block must call it. bn_eff = output columns one tile covers along N
-// (for FWD1 this is gate columns: a tile holds bn_eff gate and bn_eff up columns).
+// Copies the expert offsets into s_off[0..E] and scans the per-group tile counts into
+// tile_start[0..ng] (both shared memory). Every thread of the block must call it.
+// bn_eff = output columns one tile covers along N (for FWD1 this is gate columns: a tile
+// holds bn_eff gate and bn_eff up columns).
 __device__ __forceinline__ void build_tile_starts(const GroupedArgs& a, int mode, int bm,
-                                                  int bn_eff, int* tile_start, int* warp_sums) {
+                                                  int bn_eff, int* tile_start, int* warp_sums,
+                                                  int* s_off) {
+  if (mode != ROUTER)
+    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = __ldg(a.offsets + i);
+  __syncthreads();
   const int ng = num_groups(mode, a.E, a.S);
   const int nt = blockDim.x;
   const int per = (ng + nt - 1) / nt;
@@ -116,7 +122,7 @@ __device__ __forceinline__ void build_tile_starts(const GroupedArgs& a, int mode
   for (int i = 0; i < per; ++i) {
     const int g = g0 + i;
     if (g < ng) {
-      const GroupGeom G = group_geom(a, mode, g);
+      const GroupGeom G = group_geom(a, mode, g, s_off);
       const int t = ((G.M + bm - 1) / bm) * ((G.N + bn_eff - 1) / bn_eff);
       tile_start[g] = t;  // temporarily the count
       local += t;
@@ -175,10 +181,10 @@ struct TileCoord {
 // Tiles of a group are ordered N-tile major, M-tile minor, so that CTAs working at the same
 // time on one expert share its weight tile through L2.
 __device__ __forceinline__ TileCoord decode_tile(const GroupedArgs& a, int mode, const int* tile_start,
-                                                 int ng, int tile, int bm) {
+                                                 int ng, int tile, int bm, const int* s_off) {
   TileCoord c;
   c.g = find_group(tile_start, ng, tile);
-  c.G = group_geom(a, mode, c.g);
+  c.G = group_geom(a, mode, c.g, s_off);
   const int local = tile - tile_start[c.g];
   const int mt = (c.G.M + bm - 1) / bm;
   c.ni = local / mt;
