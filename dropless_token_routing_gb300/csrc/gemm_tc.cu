@@ -399,17 +399,32 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileCoord
     const int zc = G.shared ? G.s : G.e;
     const bool empty = G.K == 0;               // dW of an expert without rows
     if (rowc < G.M) {
+      const int nch = (min(BN, G.N - n0) + 63) / 64;
+      // software pipeline: the TMEM load of chunk c+1 is in flight while chunk c is staged
+      uint32_t u[64];
+      if (!empty) {
+        tmem_ld32(acc, *reinterpret_cast<uint32_t(*)[32]>(u));
+        tmem_ld32(acc + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+      }
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 64) {
-        if (n0 + c >= G.N) break;
-        float v[64];
+      for (int ch = 0; ch < nch; ++ch) {
+        const int c = ch * 64;
         if (!empty) {
-          tmem_ld64(acc + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            pk[q] = make_uint4(pack_bf16x2(__uint_as_float(u[8 * q]), __uint_as_float(u[8 * q + 1])),
+                               pack_bf16x2(__uint_as_float(u[8 * q + 2]), __uint_as_float(u[8 * q + 3])),
+                               pack_bf16x2(__uint_as_float(u[8 * q + 4]), __uint_as_float(u[8 * q + 5])),
+                               pack_bf16x2(__uint_as_float(u[8 * q + 6]), __uint_as_float(u[8 * q + 7])));
+          if (ch + 1 < nch) {
+            tmem_ld32(acc + c + 64, *reinterpret_cast<uint32_t(*)[32]>(u));
+            tmem_ld32(acc + c + 96, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+          }
         } else {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) v[i] = 0.f;
+          for (int q = 0; q < 8; ++q) pk[q] = make_uint4(0u, 0u, 0u, 0u);
         }
-        pack64(v, pk);
         if (lane == 0) bulk_wait_read0();      // the previous store has left the buffer
         __syncwarp();
         uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
