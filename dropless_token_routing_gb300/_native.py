@@ -74,6 +74,7 @@ _SIGS = {
     "moe_route_topk": (c_int, [P, P, c_int64, c_int32, c_int32, P, P, P, P, c_size_t, P]),
     "moe_permute": (c_int, [P, P, P, ctypes.POINTER(MoeDims), P, P, P, P, P, P, c_size_t, P]),
     "moe_permute_rows": (c_int, [P, P, ctypes.POINTER(MoeDims), P, P]),
+    "moe_permute_noalloc": (c_int, [P, P, P, ctypes.POINTER(MoeDims), P, P, P, P, P, P, P]),
     "moe_grouped_swiglu_fwd": (c_int, [P, P, P, P, P, P, P, ctypes.POINTER(MoeDims), P, P, P, P, P,
                                        P, P, c_size_t, P]),
     "moe_unpermute_combine": (c_int, [P, P, P, P, ctypes.POINTER(MoeDims), P, P]),

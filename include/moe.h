@@ -120,6 +120,20 @@ int moe_permute(const void* x, const int32_t* topk_idx, const float* topk_w, con
                 void* x_perm, int32_t* dest, int32_t* row_src, int32_t* offsets, float* w_perm,
                 void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* a2 without a workspace, for callers that cannot allocate device memory (an allocator-free
+ * runtime, a memory pool that must not grow, a process limited to the buffers it was given).
+ * The pages have no counterpart of this call. Same inputs, outputs and results as moe_permute;
+ * the permutation's scratch lives in one static device array of the library (about 1.5 MB,
+ * held by every GPU that loads the library until the process exits) instead of a workspace.
+ * Limits: T*k <= 262144 and E * ceil(T/64) <= 65536, else MOE_ERR_WORKSPACE_TOO_SMALL (nothing
+ * launched). dev_err: optional device int that receives MOE_ERR_DEVICE_EXPERT_ID for invalid
+ * ids (first error wins; the caller zeroes it), or NULL. The first call on a device looks up the
+ * array's address for that device; make it before any stream capture. Every call shares the
+ * array: calls that overlap on the GPU race, so order them on one stream. */
+int moe_permute_noalloc(const void* x, const int32_t* topk_idx, const float* topk_w,
+                        const moe_dims* dims, void* x_perm, int32_t* dest, int32_t* row_src,
+                        int32_t* offsets, float* w_perm, int* dev_err, moe_stream_t stream);
+
 /* a2 (gather-only mode, used for dY in the backward): x_perm[dest[q]] = x[q / k] for a dest
  * from moe_permute. x [T, d] -> x_perm [T*k, d]. Copies with dest < 0 are skipped. */
 int moe_permute_rows(const void* x, const int32_t* dest, const moe_dims* dims, void* x_perm,
