@@ -36,7 +36,12 @@ UNIT = "tokens/s"
 
 # DRAM traffic per launch from an ncu capture of the dominant kernel, keyed by the phase
 # name; valid only while the kernel source still hashes to src_sha256.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum (one pass)
+    # on the default workload, one launch after warm-up; see profiles/gemm_dw13_pangu_bf16.md
+    "gemm_dw13": {"bytes_per_launch": 2242334208 + 16164291328,
+                  "src_sha256": "6880e5cfbd15c1559669a96146c72968004321ef71382fe550a1ade6470aa634"},
+}
 
 
 def _peaks():

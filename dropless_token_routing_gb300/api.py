@@ -138,11 +138,12 @@ class MoELayer:
     """One dropless MoE layer: caller-owned saved activations, gradients and workspace.
 
     ``forward(x, logits_in=None)`` runs moe_layer_fwd; ``backward(dy)`` runs
-    moe_layer_bwd on the values the last forward saved.
+    moe_layer_bwd on the values the last forward saved. ``recompute=True`` keeps neither
+    the rearranged input nor h between the two (selective recompute).
     """
 
     def __init__(self, params: LayerParams, T, d, E, k, f, S=0, f_s=0, dtype=torch.bfloat16,
-                 device="cuda", logits_input=False):
+                 device="cuda", logits_input=False, recompute=False):
         self.params = params
         self.dims = make_dims(T, d, E, k, f, S, f_s, dtype)
         self.T, self.d, self.E, self.k, self.f, self.S, self.f_s = T, d, E, k, f, S, f_s
@@ -156,8 +157,10 @@ class MoELayer:
             topk_idx=emp(T, k, dt=torch.int32), topk_w=emp(T, k, dt=torch.float32),
             counts=emp(E, dt=torch.int32), offsets=emp(E + 1, dt=torch.int32),
             dest=emp(Tk, dt=torch.int32), row_src=emp(Tk, dt=torch.int32),
-            w_perm=emp(Tk, dt=torch.float32), x_perm=emp(Tk, d), z=emp(Tk, 2 * f), h=emp(Tk, f),
-            z_sh=emp(S * T, 2 * f_s) if S else None, h_sh=emp(S * T, f_s) if S else None)
+            w_perm=emp(Tk, dt=torch.float32), x_perm=None if recompute else emp(Tk, d),
+            z=emp(Tk, 2 * f), h=None if recompute else emp(Tk, f),
+            z_sh=emp(S * T, 2 * f_s) if S else None,
+            h_sh=emp(S * T, f_s) if (S and not recompute) else None)
         self.y = emp(T, d)
         self.grads = None
         self._x = None

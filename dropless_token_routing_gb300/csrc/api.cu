@@ -44,6 +44,9 @@ WsLayout ws_layout(const moe_dims& d) {
   L.hw = take(es * Tk * f);
   L.hw_sh = take(es * ST * fs);
   L.dx_sh = take(es * T * D);
+  L.x_perm_tmp = take(es * Tk * D);     // selective recompute: x_perm not kept by the caller
+  L.h_tmp = take(es * Tk * f);          // ... h (routed) not kept
+  L.h_sh_tmp = take(es * ST * fs);      // ... h (shared) not kept
   L.total = o;
   return L;
 }
@@ -470,21 +473,24 @@ int moe_layer_fwd(const moe_layer_params* params, const void* x, const float* lo
   MOE_TRY(reqT(saved->dest, t0));
   MOE_TRY(reqT(saved->row_src, t0));
   MOE_TRY(reqT(saved->w_perm, t0));
-  MOE_TRY(reqT(saved->x_perm, t0));
+  MOE_TRY(opt(saved->x_perm));   // NULL: kept in the workspace, recomputed by the backward
   MOE_TRY(reqT(saved->z, t0));
-  MOE_TRY(reqT(saved->h, t0));
+  MOE_TRY(opt(saved->h));        // NULL: kept in the workspace (the backward recomputes h from z)
   MOE_TRY(req(params->w13));
   MOE_TRY(req(params->w2));
   if (dims->S > 0) {
     MOE_TRY(req(params->ws13));
     MOE_TRY(req(params->ws2));
     MOE_TRY(reqT(saved->z_sh, t0));
-    MOE_TRY(reqT(saved->h_sh, t0));
+    MOE_TRY(opt(saved->h_sh));
   }
   MOE_TRY(check_gemm_device(dims));
   const cudaStream_t st = (cudaStream_t)stream;
   const WsLayout L = ws_layout(*dims);
   uint8_t* w = static_cast<uint8_t*>(ws);
+  void* x_perm = saved->x_perm != nullptr ? saved->x_perm : (void*)(w + L.x_perm_tmp);
+  void* h = saved->h != nullptr ? saved->h : (void*)(w + L.h_tmp);
+  void* h_sh = dims->S == 0 ? nullptr : saved->h_sh != nullptr ? saved->h_sh : (void*)(w + L.h_sh_tmp);
   if (dims->T == 0) {
     if (cudaMemsetAsync(saved->counts, 0, sizeof(int32_t) * dims->E, st) != cudaSuccess ||
         cudaMemsetAsync(saved->offsets, 0, sizeof(int32_t) * (dims->E + 1), st) != cudaSuccess)
@@ -499,17 +505,17 @@ int moe_layer_fwd(const moe_layer_params* params, const void* x, const float* lo
   if (cudaMemsetAsync(saved->counts, 0, sizeof(int32_t) * dims->E, st) != cudaSuccess) return MOE_ERR_CUDA;
   MOE_LAUNCH(launch_route_topk(scores, params->bias, dims->T, dims->E, dims->k, saved->topk_idx,
                                saved->topk_w, saved->counts, dev_info().sms, st));
-  MOE_LAUNCH(launch_permute(x, saved->topk_idx, saved->topk_w, *dims, saved->x_perm, saved->dest,
+  MOE_LAUNCH(launch_permute(x, saved->topk_idx, saved->topk_w, *dims, x_perm, saved->dest,
                             saved->row_src, saved->offsets, saved->w_perm, L, w,
                             reinterpret_cast<int*>(w + L.err), st));
   GroupedArgs a = base_args(dims, saved->offsets, reinterpret_cast<int*>(w + L.err));
-  a.x_perm = saved->x_perm; a.x = x; a.w13 = params->w13; a.w2 = params->w2;
+  a.x_perm = x_perm; a.x = x; a.w13 = params->w13; a.w2 = params->w2;
   a.ws13 = params->ws13; a.ws2 = params->ws2;
-  a.z_out = saved->z; a.h_out = saved->h; a.z_sh_out = saved->z_sh; a.h_sh_out = saved->h_sh;
+  a.z_out = saved->z; a.h_out = h; a.z_sh_out = saved->z_sh; a.h_sh_out = h_sh;
   MOE_TRY(run_grouped(FWD1, a, dims, st));
   void* y_perm = w + L.y_perm;
   void* y_sh = dims->S > 0 ? (void*)(w + L.y_sh) : nullptr;
-  a.h = saved->h; a.h_sh = saved->h_sh; a.y_perm = y_perm; a.y_sh = y_sh;
+  a.h = h; a.h_sh = h_sh; a.y_perm = y_perm; a.y_sh = y_sh;
   MOE_TRY(run_grouped(FWD2, a, dims, st));
   MOE_LAUNCH(launch_combine(y_perm, saved->dest, saved->topk_w, y_sh, nullptr, nullptr, nullptr,
                             *dims, y, st));
@@ -542,7 +548,7 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
   MOE_TRY(reqT(saved->dest, t0));
   MOE_TRY(reqT(saved->row_src, t0));
   MOE_TRY(reqT(saved->w_perm, t0));
-  MOE_TRY(reqT(saved->x_perm, t0));
+  MOE_TRY(opt(saved->x_perm));   // NULL: re-permuted from x here
   MOE_TRY(reqT(saved->z, t0));
   MOE_TRY(req(params->w13));
   MOE_TRY(req(params->w2));
@@ -601,7 +607,12 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
   MOE_LAUNCH(launch_combine(dx_perm, saved->dest, nullptr, dx_sh, saved->topk_idx, dl_tok, w_rT, *dims,
                             grads->dx, st));
   // 6. expert dW products (separate kernels from the dX chain)
-  a.x_perm = saved->x_perm; a.x = x; a.hw = hw; a.hw_sh = hw_sh;
+  const void* x_perm = saved->x_perm;
+  if (x_perm == nullptr) {  // selective recompute of the rearranged input
+    MOE_LAUNCH(launch_permute_rows(x, saved->dest, *dims, w + L.x_perm_tmp, st));
+    x_perm = w + L.x_perm_tmp;
+  }
+  a.x_perm = x_perm; a.x = x; a.hw = hw; a.hw_sh = hw_sh;
   a.dw13 = grads->dw13; a.dw2 = grads->dw2; a.dws13 = grads->dws13; a.dws2 = grads->dws2;
   MOE_TRY(run_grouped(DW2, a, dims, st));
   MOE_TRY(run_grouped(DW13, a, dims, st));

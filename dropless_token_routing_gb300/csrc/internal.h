@@ -41,6 +41,9 @@ struct WsLayout {
   size_t hw;           // [T*k, f]
   size_t hw_sh;        // [S*T, f_s]
   size_t dx_sh;        // [T, d]
+  size_t x_perm_tmp;   // [T*k, d]   x_perm when the caller does not keep it
+  size_t h_tmp;        // [T*k, f]   h when the caller does not keep it
+  size_t h_sh_tmp;     // [S*T, f_s]
   size_t total;
   int64_t n_chunks;
   int n_dgate_tiles;

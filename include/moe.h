@@ -210,12 +210,17 @@ typedef struct moe_layer_saved { /* caller-allocated; written by moe_layer_fwd, 
   int32_t* dest;     /* [T*k] */
   int32_t* row_src;  /* [T*k] */
   float* w_perm;     /* [T*k] */
-  void* x_perm;      /* [T*k, d] */
+  void* x_perm;      /* [T*k, d], or NULL: selective recompute, the backward re-permutes x */
   void* z;           /* [T*k, 2f] */
-  void* h;           /* [T*k, f] */
+  void* h;           /* [T*k, f], or NULL: not kept (the backward recomputes h from z) */
   void* z_sh;        /* [S*T, 2f_s] or NULL when S == 0 */
-  void* h_sh;        /* [S*T, f_s] or NULL when S == 0 */
+  void* h_sh;        /* [S*T, f_s], or NULL (not kept, or S == 0) */
 } moe_layer_saved;
+/* Selective recompute (Pangu Ultra MoE tech-report article, memory section: permutation and
+ * activation recomputed instead of saved; Huawei MoE training-operator article, Selective R/S):
+ * with saved->x_perm, saved->h and saved->h_sh NULL the forward keeps them in the workspace
+ * only, and the backward re-permutes x; the saved activations shrink by T*k*(d+f) + S*T*f_s
+ * elements for one extra row move of x. Results are identical. */
 
 typedef struct moe_layer_grads { /* caller-allocated outputs of moe_layer_bwd */
   void* dx;        /* [T, d]; includes the router term when w_r is given */

@@ -82,3 +82,25 @@ def test_zero_tokens_is_noop_and_zero_grads():
     assert layer.saved["counts"].sum().item() == 0 and layer.saved["offsets"].abs().sum().item() == 0
     for n in ("dw13", "dw2", "dws13", "dws2", "dw_r"):
         assert not g[n].any(), n
+
+
+def test_selective_recompute_gives_identical_results():
+    """x_perm and h not kept by the caller: the backward re-permutes x; bitwise the same."""
+    from dropless_token_routing_gb300.api import LayerParams, MoELayer
+    w = make_workload(shrink("pangu_bf16", T=700, d=512, E=16, k=4, f=256, f_s=256))
+    c, dev = w.cfg, "cuda"
+    to = lambda t: None if t is None else t.to(dev)  # noqa: E731
+    out = []
+    for rc in (False, True):
+        params = LayerParams(w13=to(w.w13), w2=to(w.w2), w_r=to(w.w_r), bias=to(w.bias),
+                             ws13=to(w.ws13), ws2=to(w.ws2))
+        layer = MoELayer(params, c["T"], c["d"], c["E"], c["k"], c["f"], c["S"], c["f_s"],
+                         torch.bfloat16, recompute=rc)
+        y = layer.forward(to(w.x)).clone()
+        g = {k_: v.clone() for k_, v in layer.backward(to(w.dy)).items() if v is not None}
+        out.append((y, g))
+    torch.cuda.synchronize()
+    (y0, g0), (y1, g1) = out
+    assert torch.equal(y0, y1)
+    for k_ in g0:
+        assert torch.equal(g0[k_], g1[k_]), k_
