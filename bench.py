@@ -369,18 +369,28 @@ def main():
     total_ms = sum(v[1] for v in trace.values())
     kernels = {}
     for name, (launches, ms) in sorted(trace.items(), key=lambda kv: -kv[1][1]):
+        # every phase is one operation per step, possibly of several launches (the dW_r
+        # partial sums and their reduction; the router's weight split and its GEMM), so
+        # the operation's work is divided by the phase's time per step
         per = ms / launches
+        per_step = ms / args.steps
         ent = {"launches_per_step": launches / args.steps, "ms_per_launch": round(per, 4),
+               "ms_per_step": round(per_step, 4),
                "share": round(ms / total_ms, 4) if total_ms else None}
         if name in flops and name != "router_gemm":
-            ach = flops[name] / (per / 1e3) / 1e12
+            ach = flops[name] / (per_step / 1e3) / 1e12
             ent.update(achieved=round(ach, 1), unit="TFLOP/s",
                        frac=round(ach / peaks["bf16_tflops_sustained"], 3))
         elif name in bytes_:
-            ach = bytes_[name] / (per / 1e3) / 1e9
+            ach = bytes_[name] / (per_step / 1e3) / 1e9
             ent.update(achieved=round(ach, 1), unit="GB/s", frac=round(ach / peaks["hbm_gbs"], 3))
         elif name == "router_gemm":
-            ent.update(achieved=round(flops[name] / (per / 1e3) / 1e12, 2), unit="TFLOP/s (fp32 FMA)")
+            if cfg["dtype"] == "f32":
+                ent.update(achieved=round(flops[name] / (per_step / 1e3) / 1e12, 2),
+                           unit="TFLOP/s (fp32 FMA)")
+            else:   # three bf16 parts of the fp32 weight, each a full product on the tensor cores
+                ent.update(achieved=round(3 * flops[name] / (per_step / 1e3) / 1e12, 1),
+                           unit="TFLOP/s (bf16, 3-part weight split, executed)")
         kernels[name] = ent
     dom = max(trace.items(), key=lambda kv: kv[1][1])[0]
     dl, dms = trace[dom]

@@ -120,6 +120,20 @@ def route_topk_bwd(topk_idx, topk_w, dgate, E, dlogits, stream=None):
                                        _s(stream)), "moe_route_topk_bwd")
 
 
+def route_balance(logits, bias, counts, k, alpha, prob_mean, aux_loss, ws: Workspace, stream=None):
+    T, E = logits.shape
+    N.check(N.lib().moe_route_balance(_p(logits), _p(bias), _p(counts), T, E, k, float(alpha),
+                                      _p(prob_mean), _p(aux_loss), ws.ptr, ws.nbytes, _s(stream)),
+            "moe_route_balance")
+
+
+def route_balance_bwd(logits, bias, counts, k, alpha, grad, dlogits, stream=None):
+    T, E = logits.shape
+    N.check(N.lib().moe_route_balance_bwd(_p(logits), _p(bias), _p(counts), T, E, k, float(alpha),
+                                          float(grad), _p(dlogits), _s(stream)),
+            "moe_route_balance_bwd")
+
+
 @dataclass
 class LayerParams:
     w13: torch.Tensor

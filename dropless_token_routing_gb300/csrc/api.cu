@@ -437,6 +437,40 @@ int moe_grouped_bwd_dw(const void* x_perm, const void* x, const void* hw, const 
   return MOE_OK;
 }
 
+int moe_route_balance(const float* logits, const float* bias, const int32_t* counts, int64_t T,
+                      int32_t E, int32_t k, float alpha, float* prob_mean, float* aux_loss, void* ws,
+                      size_t ws_bytes, moe_stream_t stream) {
+  if (E < 1 || E > kMaxE || T < 1 || T > (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
+  if (k < 1 || k > E || k > kMaxK) return MOE_ERR_BAD_TOPK;
+  if (ws == nullptr) return MOE_ERR_NULL_POINTER;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < 256 + sizeof(float) * (size_t)balance_blocks(T) * E) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  MOE_TRY(req(logits));
+  MOE_TRY(opt(bias));
+  MOE_TRY(req(counts));
+  MOE_TRY(opt(prob_mean));
+  MOE_TRY(req(aux_loss));
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
+  MOE_LAUNCH(launch_balance(logits, bias, counts, T, E, k, alpha, part, prob_mean, aux_loss,
+                            (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+int moe_route_balance_bwd(const float* logits, const float* bias, const int32_t* counts, int64_t T,
+                          int32_t E, int32_t k, float alpha, float grad, float* dlogits,
+                          moe_stream_t stream) {
+  if (E < 1 || E > kMaxE || T < 0 || T > (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
+  if (k < 1 || k > E || k > kMaxK) return MOE_ERR_BAD_TOPK;
+  if (T == 0) return MOE_OK;
+  MOE_TRY(req(logits));
+  MOE_TRY(opt(bias));
+  MOE_TRY(req(counts));
+  MOE_TRY(req(dlogits));
+  const double scale = (double)grad * alpha * E / ((double)T * (double)T * (double)k);
+  MOE_LAUNCH(launch_balance_bwd(logits, bias, counts, T, E, (float)scale, dlogits, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
 int moe_route_topk_bwd(const int32_t* topk_idx, const float* topk_w, const float* dgate, int64_t T,
                        int32_t E, int32_t k, float* dlogits, moe_stream_t stream) {
   if (E < 1 || E > kMaxE || T < 0) return MOE_ERR_BAD_DIMS;

@@ -71,6 +71,12 @@ cudaError_t launch_combine(const void* y_perm, const int32_t* dest, const float*
 cudaError_t launch_router_split(const float* w_r, int d, int E, void* w_split, cudaStream_t st);
 cudaError_t launch_router_reduce(const float* part, int64_t T, int E, int nsplit, float* logits,
                                  cudaStream_t st);
+int balance_blocks(int64_t T);
+cudaError_t launch_balance(const float* logits, const float* bias, const int32_t* counts, int64_t T,
+                           int E, int k, float alpha, float* part, float* prob_mean, float* aux_loss,
+                           cudaStream_t st);
+cudaError_t launch_balance_bwd(const float* logits, const float* bias, const int32_t* counts,
+                               int64_t T, int E, float scale, float* dlogits, cudaStream_t st);
 cudaError_t launch_transpose_f32(const float* in, int rows, int cols, float* out, cudaStream_t st);
 cudaError_t launch_dwr(const void* x, const int32_t* row_src, const float* dl_perm,
                        const int32_t* offsets, const moe_dims& dm, float* part, float* dw_r,

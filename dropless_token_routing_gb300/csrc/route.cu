@@ -229,6 +229,139 @@ __global__ void router_reduce_kernel(const float* __restrict__ part, int64_t T, 
   }
 }
 
+// ---------------------------------------------------------------- load-balance statistics
+// Mean full-softmax probability per expert. One warp per token (fixed token order per warp);
+// each lane keeps fp32 sums for its experts, then the block sums its warps in order and writes
+// one partial row per block; balance_final_kernel sums the block rows in order.
+template <int V>
+__global__ void __launch_bounds__(256) balance_partial_kernel(const float* __restrict__ logits,
+                                                              const float* __restrict__ bias,
+                                                              int64_t T, int E,
+                                                              float* __restrict__ part) {
+  __shared__ float wsum[8][kMaxE];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < T; t += (int64_t)gridDim.x * nw) {
+    float v[V];
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = -FLT_MAX;
+      if (e < E) {
+        float s = __ldg(logits + t * E + e);
+        if (bias != nullptr) s = s + __ldg(bias + e);
+        v[i] = s;
+        m = fmaxf(m, s);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      v[i] = (lane + 32 * i < E) ? expf(v[i] - m) : 0.f;
+      z += v[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const float inv = 1.f / z;
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = fmaf(v[i], inv, acc[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < V; ++i)
+    if (lane + 32 * i < E) wsum[warp][lane + 32 * i] = acc[i];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float s = 0.f;
+    for (int w = 0; w < nw; ++w) s += wsum[w][e];
+    part[(int64_t)blockIdx.x * E + e] = s;
+  }
+}
+
+// P_e = (sum over block rows) / T;  L_aux = alpha * E / (T * k) * sum_e counts_e * P_e.
+__global__ void __launch_bounds__(1024) balance_final_kernel(const float* __restrict__ part,
+                                                             int nblocks, const int32_t* __restrict__ counts,
+                                                             int64_t T, int E, int k, float alpha,
+                                                             float* __restrict__ prob_mean,
+                                                             float* __restrict__ aux_loss) {
+  __shared__ float red[32];
+  const int e = threadIdx.x;
+  float term = 0.f;
+  if (e < E) {
+    float s = 0.f;
+    for (int b = 0; b < nblocks; ++b) s += part[(int64_t)b * E + e];
+    const float P = s / (float)T;
+    if (prob_mean != nullptr) prob_mean[e] = P;
+    term = (float)counts[e] * P;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+  if (lane == 0) red[warp] = term;
+  __syncthreads();
+  if (threadIdx.x == 0 && aux_loss != nullptr) {
+    float s = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
+    aux_loss[0] = alpha * (float)E / ((float)T * (float)k) * s;
+  }
+}
+
+// dlogits[t, e] += scale * p_te * (counts_e - sum_e' counts_e' p_te'),
+// scale = grad * alpha * E / (T * T * k). One warp per token.
+template <int V>
+__global__ void __launch_bounds__(256) balance_bwd_kernel(const float* __restrict__ logits,
+                                                          const float* __restrict__ bias,
+                                                          const int32_t* __restrict__ counts,
+                                                          int64_t T, int E, float scale,
+                                                          float* __restrict__ dlogits) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < T; t += (int64_t)gridDim.x * nw) {
+    float v[V], c[V];
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = -FLT_MAX;
+      c[i] = 0.f;
+      if (e < E) {
+        float s = __ldg(logits + t * E + e);
+        if (bias != nullptr) s = s + __ldg(bias + e);
+        v[i] = s;
+        c[i] = (float)__ldg(counts + e);
+        m = fmaxf(m, s);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      v[i] = (lane + 32 * i < E) ? expf(v[i] - m) : 0.f;
+      z += v[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const float inv = 1.f / z;
+    float cp = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      v[i] *= inv;
+      cp = fmaf(c[i], v[i], cp);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cp += __shfl_xor_sync(0xffffffffu, cp, o);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) dlogits[t * E + e] += scale * v[i] * (c[i] - cp);
+    }
+  }
+}
+
 // out[c][r] = in[r][c] for an fp32 [rows][cols] matrix.
 __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int cols,
                                      float* __restrict__ out) {
@@ -368,6 +501,47 @@ cudaError_t launch_router_reduce(const float* part, int64_t T, int E, int nsplit
   if (blocks > 4096) blocks = 4096;
   TraceScope ts(TP_ROUTER_GEMM, st);
   router_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(part, T, E, (E + 31) & ~31, nsplit, logits);
+  return cudaGetLastError();
+}
+
+int balance_blocks(int64_t T) {
+  int64_t b = (T + 7) / 8;
+  return (int)(b < 256 ? (b < 1 ? 1 : b) : 256);
+}
+
+#define MOE_V_DISPATCH(E, CALL)            \
+  do {                                     \
+    const int V_ = ((E) + 31) / 32;        \
+    if (V_ <= 1) { constexpr int VV = 1; CALL; } \
+    else if (V_ <= 2) { constexpr int VV = 2; CALL; } \
+    else if (V_ <= 4) { constexpr int VV = 4; CALL; } \
+    else if (V_ <= 8) { constexpr int VV = 8; CALL; } \
+    else if (V_ <= 16) { constexpr int VV = 16; CALL; } \
+    else { constexpr int VV = 32; CALL; } \
+  } while (0)
+
+cudaError_t launch_balance(const float* logits, const float* bias, const int32_t* counts, int64_t T,
+                           int E, int k, float alpha, float* part, float* prob_mean, float* aux_loss,
+                           cudaStream_t st) {
+  const int nb = balance_blocks(T);
+  {
+    TraceScope ts(TP_MISC, st);
+    MOE_V_DISPATCH(E, (balance_partial_kernel<VV><<<nb, 256, 0, st>>>(logits, bias, T, E, part)));
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  TraceScope ts(TP_MISC, st);
+  balance_final_kernel<<<1, 1024, 0, st>>>(part, nb, counts, T, E, k, alpha, prob_mean, aux_loss);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_balance_bwd(const float* logits, const float* bias, const int32_t* counts,
+                               int64_t T, int E, float scale, float* dlogits, cudaStream_t st) {
+  int64_t blocks = (T + 7) / 8;
+  if (blocks > 65535) blocks = 65535;
+  TraceScope ts(TP_MISC, st);
+  MOE_V_DISPATCH(E, (balance_bwd_kernel<VV><<<(unsigned)blocks, 256, 0, st>>>(logits, bias, counts, T, E,
+                                                                               scale, dlogits)));
   return cudaGetLastError();
 }
 

@@ -191,6 +191,26 @@ int moe_grouped_bwd_dw(const void* x_perm, const void* x, const void* hw, const 
 int moe_route_topk_bwd(const int32_t* topk_idx, const float* topk_w, const float* dgate,
                        int64_t T, int32_t E, int32_t k, float* dlogits, moe_stream_t stream);
 
+/* Load-balance statistics (Pangu Ultra MoE tech-report article, load-balancing section:
+ * sequence-level, global-batch and EP-group balance losses; MoE operator optimisation page,
+ * section 4.3: a load term added to the loss). The pages give no formula; the reading taken is
+ * the usual auxiliary loss over one micro-batch (a sequence of T tokens):
+ *   P_e = (1/T) sum_t softmax(s_t)_e      (full softmax of the scores s = logits + bias)
+ *   f_e = counts_e / (T k)                 (share of the token copies routed to e)
+ *   L_aux = alpha * E * sum_e f_e P_e
+ * logits [T][E] fp32, bias [E] or NULL, counts [E] int32 (from moe_route_topk) ->
+ * prob_mean [E] fp32 (or NULL), aux_loss [1] fp32 (device). Fixed-order reductions
+ * (deterministic). ws: >= 256 + 4*E*min(256, ceil(T/8)) bytes, 256-byte aligned. T >= 1. */
+int moe_route_balance(const float* logits, const float* bias, const int32_t* counts, int64_t T,
+                      int32_t E, int32_t k, float alpha, float* prob_mean, float* aux_loss, void* ws,
+                      size_t ws_bytes, moe_stream_t stream);
+
+/* Gradient of grad * L_aux w.r.t. the scores, ADDED into dlogits [T][E] (counts constant):
+ *   dlogits[t,e] += grad * alpha * E / (T*T*k) * p_te * (counts_e - sum_e' counts_e' p_te'). */
+int moe_route_balance_bwd(const float* logits, const float* bias, const int32_t* counts, int64_t T,
+                          int32_t E, int32_t k, float alpha, float grad, float* dlogits,
+                          moe_stream_t stream);
+
 /* ---------------------------------------------------------------- whole layer */
 typedef struct moe_layer_params {
   const float* w_r;  /* [d][E] fp32, or NULL when the caller passes logits_in */

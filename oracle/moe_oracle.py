@@ -52,6 +52,7 @@ __all__ = [
     "silu", "silu_grad", "router_logits", "selection_scores", "route_topk",
     "expert_counts", "expert_offsets", "permutation", "swiglu_rows",
     "layer_forward", "layer_backward", "router_backward", "as_f64",
+    "balance_loss", "balance_loss_grad", "coefficient_of_variation",
 ]
 
 
@@ -288,3 +289,42 @@ def layer_backward(x, idx, w, fwd, dy, w13, w2, ws13=None, ws2=None, w_r=None):
     return dict(dx=dx, dw13=dw13, dw2=dw2, dws13=dws13, dws2=dws2, dgate=dgate,
                 dscores=dscores, dw_r=dw_r, dz=dz, dx_perm=dx_perm,
                 dgate_perm=dgate_perm, dy_perm=dy_perm)
+
+
+# ----------------------------------------------------------------------------- load balance
+# The Pangu Ultra MoE tech-report article (rjtj.cn, load-balancing section) lists auxiliary
+# balance losses at sequence, global-batch (DP group) and EP-group level without formulas; the
+# CANN MoE page (gtnt.cn, section 4.3) adds a load term to the loss. Reading taken: the usual
+# form L_aux = alpha * E * sum_e f_e * P_e over one micro-batch (a sequence of T tokens), with
+# f_e = counts_e / (T k) the share of token copies routed to expert e and P_e the mean over
+# tokens of the full softmax of the scores; the counts are constants of the gradient.
+
+def _softmax_rows(scores):
+    s = np.asarray(scores, np.float64)
+    m = s.max(axis=1, keepdims=True)
+    ex = np.exp(s - m)
+    return ex / ex.sum(axis=1, keepdims=True)
+
+
+def balance_loss(scores, counts, k, alpha):
+    """Returns (P [E] mean softmax probability per expert, L_aux)."""
+    p = _softmax_rows(scores)
+    T, E = p.shape
+    P = p.mean(axis=0)
+    f = np.asarray(counts, np.float64) / (T * k)
+    return P, alpha * E * float(np.sum(f * P))
+
+
+def balance_loss_grad(scores, counts, k, alpha):
+    """d L_aux / d scores [T, E] with the counts held constant."""
+    p = _softmax_rows(scores)
+    T, E = p.shape
+    f = np.asarray(counts, np.float64) / (T * k)
+    inner = (p * f[None, :]).sum(axis=1, keepdims=True)
+    return alpha * E / T * p * (f[None, :] - inner)
+
+
+def coefficient_of_variation(counts):
+    """std / mean of the per-expert loads (the CANN page's cv(experts_load))."""
+    c = np.asarray(counts, np.float64)
+    return float(c.std() / c.mean())

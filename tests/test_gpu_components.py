@@ -153,3 +153,45 @@ def test_route_topk_bwd_matches_oracle():
     np.put_along_axis(ref, idx, O.router_backward(gate.astype(np.float32).astype(np.float64),
                                                   dgate.double().numpy()), axis=1)
     assert np.linalg.norm(out.cpu().double().numpy() - ref) / np.linalg.norm(ref) <= 1e-5
+
+
+def test_balance_statistics_and_gradient_match_oracle():
+    """moe_route_balance / moe_route_balance_bwd against the oracle's auxiliary balance loss."""
+    A = _api()
+    T, E, k, alpha = 1000, 64, 6, 0.01
+    g = torch.Generator().manual_seed(21)
+    L = torch.randn(T, E, generator=g) * 2
+    bias = torch.randn(E, generator=g) * 0.5
+    s32 = O.selection_scores(L.numpy(), bias.numpy())
+    idx, _ = O.route_topk(s32, k)
+    counts = O.expert_counts(idx, E)
+    P_ref, L_ref = O.balance_loss(s32, counts, k, alpha)
+    dims = A.make_dims(T, 64, E, k, 64, dtype=torch.float32)
+    ws = A.Workspace(dims)
+    Lg, bg = L.cuda(), bias.cuda()
+    cg = torch.as_tensor(counts, dtype=torch.int32).cuda()
+    P = torch.empty(E, device="cuda")
+    aux = torch.empty(1, device="cuda")
+    for _ in range(2):   # deterministic: the same bits twice
+        A.route_balance(Lg, bg, cg, k, alpha, P, aux, ws)
+        torch.cuda.synchronize()
+        if _ == 0:
+            P0, aux0 = P.clone(), aux.clone()
+    assert torch.equal(P, P0) and torch.equal(aux, aux0)
+    assert np.linalg.norm(P.cpu().double().numpy() - P_ref) / np.linalg.norm(P_ref) <= 1e-5
+    assert abs(aux.item() - L_ref) / abs(L_ref) <= 1e-5
+    # into zeros: the added term alone, compared with the oracle's gradient
+    d0 = torch.zeros(T, E, device="cuda")
+    A.route_balance_bwd(Lg, bg, cg, k, alpha, 1.7, d0)
+    torch.cuda.synchronize()
+    ref = 1.7 * O.balance_loss_grad(s32, counts, k, alpha)
+    g0 = d0.cpu().double().numpy()
+    assert np.linalg.norm(g0 - ref) / np.linalg.norm(ref) <= 1e-5
+    # into an existing gradient: the call accumulates (one fp32 add, possibly fused)
+    base = torch.randn(T, E, generator=g)
+    d = base.clone().cuda()
+    A.route_balance_bwd(Lg, bg, cg, k, alpha, 1.7, d)
+    torch.cuda.synchronize()
+    expect = base + d0.cpu()
+    tol = 2 * torch.finfo(torch.float32).eps * (base.abs() + d0.cpu().abs()) + 1e-38
+    assert torch.all((d.cpu() - expect).abs() <= tol)

@@ -317,3 +317,40 @@ def test_token_permutation_and_expert_relabelling_invariance():
     idx3, _, fwd3 = _oracle_layer(x, w_r[:, inv], w13[inv], w2[inv], ws13, ws2, k)
     np.testing.assert_allclose(fwd3["y"], fwd["y"], rtol=1e-12, atol=1e-12)
     assert sorted(fwd3["counts"].tolist()) == sorted(fwd["counts"].tolist())
+
+
+# ---------------------------------------------------------------- load-balance statistics
+def test_balance_loss_closed_forms():
+    T, E, k = 64, 8, 2
+    s = np.zeros((T, E))                              # uniform router: P_e = 1/E
+    counts = np.full(E, T * k // E)                   # perfectly balanced loads: f_e = 1/E
+    P, L = O.balance_loss(s, counts, k, alpha=0.01)
+    np.testing.assert_allclose(P, 1.0 / E, rtol=1e-15)
+    np.testing.assert_allclose(L, 0.01, rtol=1e-14)   # alpha * E * E * (1/E)(1/E) = alpha
+    assert O.coefficient_of_variation(counts) == 0.0
+    # all copies on one expert with probability one there: L = alpha * E
+    s = np.full((T, E), -1e3)
+    s[:, 3] = 0.0
+    counts = np.zeros(E)
+    counts[3] = T * k
+    _, L = O.balance_loss(s, counts, k, alpha=0.5)
+    np.testing.assert_allclose(L, 0.5 * E, rtol=1e-12)
+    np.testing.assert_allclose(O.coefficient_of_variation(counts), np.sqrt(E - 1), rtol=1e-12)
+
+
+def test_balance_loss_gradient_central_differences():
+    rng = np.random.default_rng(12)
+    T, E, k = 9, 6, 2
+    s = rng.standard_normal((T, E))
+    counts = rng.integers(0, 5, E)
+    g = O.balance_loss_grad(s, counts, k, alpha=0.3)
+    num = np.zeros_like(s)
+    h = 1e-6
+    for t in range(T):
+        for e in range(E):
+            sp, sm = s.copy(), s.copy()
+            sp[t, e] += h
+            sm[t, e] -= h
+            num[t, e] = (O.balance_loss(sp, counts, k, 0.3)[1] - O.balance_loss(sm, counts, k, 0.3)[1]) / (2 * h)
+    assert np.linalg.norm(num - g) / np.linalg.norm(g) < 1e-7
+    np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-14)   # softmax Jacobian rows sum to 0
