@@ -200,6 +200,48 @@ def cpu_baseline(w, logits32, n_tokens):
                       f"({n_exp} routed experts they use + shared, full d/f), {dt:.1f} s"}
 
 
+# --------------------------------------------------------------------------- drop-and-pad
+def drop_and_pad(factors, params, cfg, w, counts, args, stream):
+    """The comparison the pages draw: the same layer step in the drop-and-pad variant, every
+    expert given C = ceil(cf * T * k / E) rows (overflow copies dropped, short experts
+    padded). Timed like the dropless step, same workload, on this rank only."""
+    import math
+    import torch
+    from dropless_token_routing_gb300.api import MoELayer, get_device_error
+    T, k, E = cfg["T"], cfg["k"], cfg["E"]
+    out = []
+    for cf in factors:
+        C = max(1, math.ceil(cf * T * k / E))
+        lay = MoELayer(params, T, cfg["d"], E, k, cfg["f"], cfg["S"], cfg["f_s"], w.torch_dtype,
+                       device=w.x.device, logits_input=w.logits_in is not None, capacity=C)
+        lay.alloc_grads()
+
+        def step():
+            lay.forward(w.x, w.logits_in)
+            lay.backward(w.dy)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        if get_device_error(lay.ws) != 0:
+            raise RuntimeError("device error in the drop-and-pad run")
+        ms = a.elapsed_time(b) / args.steps
+        kept = sum(min(c, C) for c in counts)
+        out.append({"capacity_factor": cf, "capacity": C, "value": round(T / (ms / 1e3), 1),
+                    "unit": UNIT, "ms_per_step": round(ms, 3),
+                    "dropped_copy_fraction": round(1 - kept / (T * k), 4),
+                    "padding_row_fraction": round(1 - kept / (E * C), 4)})
+        del lay
+        torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -212,6 +254,9 @@ def main():
     ap.add_argument("--oracle-tokens", type=int, default=4)
     ap.add_argument("--shrink", default="", help="smaller case of the same recipe, e.g. T=512,E=16 "
                                                   "(for profiler captures; not a bench line)")
+    ap.add_argument("--drop-pad", default="1.0,1.25",
+                    help="capacity factors of the drop-and-pad comparison runs (rank 0, after the "
+                         "dropless measurement; empty to skip)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -432,6 +477,9 @@ def main():
     if not args.no_cpu_baseline and world == 1:
         logits32 = (li if li is not None else layer.saved["logits"]).cpu().numpy()
         line["cpu_baseline"] = cpu_baseline(w, logits32, args.oracle_tokens)
+    factors = [float(v) for v in args.drop_pad.split(",") if v.strip()]
+    if factors:
+        line["drop_and_pad"] = drop_and_pad(factors, params, cfg, w, cnt, args, stream)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

@@ -31,8 +31,15 @@ def _dt(dtype) -> int:
     raise ValueError(f"unsupported dtype {dtype}")
 
 
-def make_dims(T, d, E, k, f, S=0, f_s=0, dtype=torch.bfloat16) -> N.MoeDims:
-    return N.MoeDims(int(T), int(d), int(E), int(k), int(f), int(S), int(f_s) if S else 0, _dt(dtype))
+def make_dims(T, d, E, k, f, S=0, f_s=0, dtype=torch.bfloat16, capacity=0) -> N.MoeDims:
+    """capacity = 0: dropless; C > 0: drop-and-pad with C rows per expert."""
+    return N.MoeDims(int(T), int(d), int(E), int(k), int(f), int(S), int(f_s) if S else 0, _dt(dtype),
+                     int(capacity))
+
+
+def perm_rows(dims: N.MoeDims) -> int:
+    """Rows of the permuted buffers: T*k dropless, E*C with a capacity C."""
+    return dims.E * dims.capacity if dims.capacity > 0 else dims.T * dims.k
 
 
 class Workspace:
@@ -153,16 +160,18 @@ class MoELayer:
 
     ``forward(x, logits_in=None)`` runs moe_layer_fwd; ``backward(dy)`` runs
     moe_layer_bwd on the values the last forward saved. ``recompute=True`` keeps neither
-    the rearranged input nor h between the two (selective recompute).
+    the rearranged input nor h between the two (selective recompute). ``capacity=C > 0``
+    runs the drop-and-pad variant with C rows per expert instead of the dropless layer.
     """
 
     def __init__(self, params: LayerParams, T, d, E, k, f, S=0, f_s=0, dtype=torch.bfloat16,
-                 device="cuda", logits_input=False, recompute=False):
+                 device="cuda", logits_input=False, recompute=False, capacity=0):
         self.params = params
-        self.dims = make_dims(T, d, E, k, f, S, f_s, dtype)
+        self.dims = make_dims(T, d, E, k, f, S, f_s, dtype, capacity)
         self.T, self.d, self.E, self.k, self.f, self.S, self.f_s = T, d, E, k, f, S, f_s
         self.dtype = dtype
         Tk = T * k
+        R = perm_rows(self.dims)
         dev = device
         emp = lambda *shape, dt=dtype: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
         self.ws = Workspace(self.dims, device=dev)
@@ -170,9 +179,9 @@ class MoELayer:
             logits=None if logits_input else emp(T, E, dt=torch.float32),
             topk_idx=emp(T, k, dt=torch.int32), topk_w=emp(T, k, dt=torch.float32),
             counts=emp(E, dt=torch.int32), offsets=emp(E + 1, dt=torch.int32),
-            dest=emp(Tk, dt=torch.int32), row_src=emp(Tk, dt=torch.int32),
-            w_perm=emp(Tk, dt=torch.float32), x_perm=None if recompute else emp(Tk, d),
-            z=emp(Tk, 2 * f), h=None if recompute else emp(Tk, f),
+            dest=emp(Tk, dt=torch.int32), row_src=emp(R, dt=torch.int32),
+            w_perm=emp(R, dt=torch.float32), x_perm=None if recompute else emp(R, d),
+            z=emp(R, 2 * f), h=None if recompute else emp(R, f),
             z_sh=emp(S * T, 2 * f_s) if S else None,
             h_sh=emp(S * T, f_s) if (S and not recompute) else None)
         self.y = emp(T, d)

@@ -20,6 +20,7 @@ WsLayout ws_layout(const moe_dims& d) {
   };
   const size_t es = elt_bytes(d.dtype);
   const size_t T = (size_t)d.T, Tk = (size_t)d.T * d.k, E = d.E, D = d.d, f = d.f;
+  const size_t R = (size_t)perm_rows(d);   // rows of the permuted buffers
   const size_t ST = (size_t)d.S * T, fs = d.f_s;
   L.n_chunks = (d.T + kChunk - 1) / kChunk;
   L.n_dgate_tiles = simt_dgate_tiles(d.f) > tc_dgate_tiles(d.f) ? simt_dgate_tiles(d.f)
@@ -28,7 +29,7 @@ WsLayout ws_layout(const moe_dims& d) {
   L.chunk_hist = take(4 * E * (size_t)L.n_chunks);
   L.chunk_base = take(4 * E * (size_t)L.n_chunks);
   L.local_rank = take(4 * Tk);
-  L.dgate_part = take(4 * (size_t)L.n_dgate_tiles * Tk);
+  L.dgate_part = take(4 * (size_t)L.n_dgate_tiles * R);
   L.dl_perm = take(4 * Tk);
   L.dl_tok = take(4 * Tk);
   L.dgate = take(4 * Tk);
@@ -36,17 +37,21 @@ WsLayout ws_layout(const moe_dims& d) {
   L.dwr_part = take(4 * (size_t)kDwrSplit * E * D);
   L.w_split = take(2 * 3 * E * D);
   L.router_part = take(4 * (size_t)kRouterSplit * T * ((E + 31) & ~size_t(31)));
-  L.y_perm = take(es * Tk * D);
+  L.y_perm = take(es * R * D);
   L.y_sh = take(es * T * D);
-  L.dy_perm = take(es * Tk * D);
-  L.dz = take(es * Tk * 2 * f);
+  L.dy_perm = take(es * R * D);
+  L.dz = take(es * R * 2 * f);
   L.dz_sh = take(es * ST * 2 * fs);
-  L.hw = take(es * Tk * f);
+  L.hw = take(es * R * f);
   L.hw_sh = take(es * ST * fs);
   L.dx_sh = take(es * T * D);
-  L.x_perm_tmp = take(es * Tk * D);     // selective recompute: x_perm not kept by the caller
-  L.h_tmp = take(es * Tk * f);          // ... h (routed) not kept
+  L.x_perm_tmp = take(es * R * D);      // selective recompute: x_perm not kept by the caller
+  L.h_tmp = take(es * R * f);           // ... h (routed) not kept
   L.h_sh_tmp = take(es * ST * fs);      // ... h (shared) not kept
+  const bool cap = d.capacity > 0;
+  L.dest_full = take(cap ? 4 * Tk : 0);
+  L.row_src_full = take(cap ? 4 * Tk : 0);
+  L.offsets_full = take(cap ? 4 * (E + 1) : 0);
   L.total = o;
   return L;
 }
@@ -106,7 +111,8 @@ int check_dims(const moe_dims* d) {
   if (d->S > 0 && d->f_s < 1) return MOE_ERR_BAD_DIMS;
   const int unit = d->dtype == MOE_BF16 ? 64 : 8;
   if (d->d % unit != 0 || d->f % unit != 0 || (d->S > 0 && d->f_s % unit != 0)) return MOE_ERR_BAD_DIMS;
-  const int64_t rows = d->T * (int64_t)d->k + (int64_t)d->S * d->T;
+  if (d->capacity < 0 || (int64_t)d->capacity * d->E >= (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
+  const int64_t rows = d->T * (int64_t)d->k + perm_rows(*d) + (int64_t)d->S * d->T;
   if (d->T > (int64_t)0x7fffffff || rows >= (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
   return MOE_OK;
 }
@@ -129,7 +135,7 @@ GroupedArgs base_args(const moe_dims* d, const int32_t* offsets, int* err) {
   GroupedArgs a;
   memset(&a, 0, sizeof(a));
   a.T = d->T;
-  a.Tk = d->T * d->k;
+  a.Tk = perm_rows(*d);     // rows of the permuted buffers
   a.d = d->d;
   a.E = d->E;
   a.k = d->k;
@@ -289,6 +295,9 @@ int moe_permute(const void* x, const int32_t* topk_idx, const float* topk_w, con
   uint8_t* w = static_cast<uint8_t*>(ws);
   MOE_LAUNCH(launch_permute(x, topk_idx, topk_w, *dims, x_perm, dest, row_src, offsets, w_perm, L, w,
                             reinterpret_cast<int*>(w + L.err), st));
+  if (dims->capacity > 0)
+    MOE_LAUNCH(launch_pad_rows(x_perm, dims->d, dims->dtype, reinterpret_cast<int32_t*>(w + L.offsets_full),
+                               dims->E, dims->capacity, row_src, w_perm, st));
   return MOE_OK;
 }
 
@@ -395,7 +404,7 @@ int moe_grouped_bwd_dx(const void* dy_perm, const void* dy, const void* z, const
   a.dgate_part = reinterpret_cast<float*>(w + L.dgate_part);
   MOE_TRY(run_grouped(BWD2T, a, dims, st));
   MOE_LAUNCH(launch_route_bwd(nullptr, w_perm, nullptr, a.dgate_part, dgate_tiles(dims), a.Tk, dest,
-                              dims->T, dims->E, dims->k, dgate, nullptr, nullptr, nullptr, st));
+                              nullptr, dims->T, dims->E, dims->k, dgate, nullptr, nullptr, nullptr, st));
   a.dz = dz; a.dz_sh = dz_sh; a.dx_perm = dx_perm; a.dx_sh = dx_sh;
   MOE_TRY(run_grouped(BWD1T, a, dims, st));
   return MOE_OK;
@@ -480,8 +489,8 @@ int moe_route_topk_bwd(const int32_t* topk_idx, const float* topk_w, const float
   MOE_TRY(req(topk_w));
   MOE_TRY(req(dgate));
   MOE_TRY(req(dlogits));
-  MOE_LAUNCH(launch_route_bwd(topk_idx, topk_w, dgate, nullptr, 0, 0, nullptr, T, E, k, nullptr,
-                              dlogits, nullptr, nullptr, (cudaStream_t)stream));
+  MOE_LAUNCH(launch_route_bwd(topk_idx, topk_w, dgate, nullptr, 0, 0, nullptr, nullptr, T, E, k,
+                              nullptr, dlogits, nullptr, nullptr, (cudaStream_t)stream));
   return MOE_OK;
 }
 
@@ -542,6 +551,9 @@ int moe_layer_fwd(const moe_layer_params* params, const void* x, const float* lo
   MOE_LAUNCH(launch_permute(x, saved->topk_idx, saved->topk_w, *dims, x_perm, saved->dest,
                             saved->row_src, saved->offsets, saved->w_perm, L, w,
                             reinterpret_cast<int*>(w + L.err), st));
+  if (dims->capacity > 0)
+    MOE_LAUNCH(launch_pad_rows(x_perm, dims->d, dims->dtype, reinterpret_cast<int32_t*>(w + L.offsets_full),
+                               dims->E, dims->capacity, saved->row_src, saved->w_perm, st));
   GroupedArgs a = base_args(dims, saved->offsets, reinterpret_cast<int*>(w + L.err));
   a.x_perm = x_perm; a.x = x; a.w13 = params->w13; a.w2 = params->w2;
   a.ws13 = params->ws13; a.ws2 = params->ws2;
@@ -615,8 +627,23 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
   float* dl_perm = reinterpret_cast<float*>(w + L.dl_perm);
   float* dgate = reinterpret_cast<float*>(w + L.dgate);
 
+  // 0. drop-and-pad: the dropless positions of every copy (the router gradient reaches the
+  //    dropped copies too) and the expert counts that locate the padding rows
+  const bool cap = dims->capacity > 0;
+  int32_t* dest_full = reinterpret_cast<int32_t*>(w + L.dest_full);
+  int32_t* row_src_full = reinterpret_cast<int32_t*>(w + L.row_src_full);
+  int32_t* offsets_full = reinterpret_cast<int32_t*>(w + L.offsets_full);
+  if (cap) {
+    moe_dims full = *dims;
+    full.capacity = 0;
+    MOE_LAUNCH(launch_permute(nullptr, saved->topk_idx, nullptr, full, nullptr, dest_full, row_src_full,
+                              offsets_full, nullptr, L, w, err, st));
+  }
   // 1. rearrange dY like x
   MOE_LAUNCH(launch_permute_rows(dy, saved->dest, *dims, dy_perm, st));
+  if (cap)
+    MOE_LAUNCH(launch_pad_rows(dy_perm, dims->d, dims->dtype, offsets_full, dims->E, dims->capacity,
+                               nullptr, nullptr, st));
   // 2. expert dX chain, first half: D = dY W2, dgate partials, dz, hw
   GroupedArgs a = base_args(dims, saved->offsets, err);
   a.dy_perm = dy_perm; a.dy = dy; a.z = saved->z; a.z_sh = saved->z_sh;
@@ -627,8 +654,8 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
   MOE_TRY(run_grouped(BWD2T, a, dims, st));
   // 3. dgate -> score gradient (dlogits), in token and permuted order
   MOE_LAUNCH(launch_route_bwd(saved->topk_idx, saved->topk_w, nullptr, dgate_part, dgate_tiles(dims),
-                              a.Tk, saved->dest, dims->T, dims->E, dims->k, dgate, grads->dlogits,
-                              dl_tok, dl_perm, st));
+                              a.Tk, saved->dest, cap ? dest_full : saved->dest, dims->T, dims->E,
+                              dims->k, dgate, grads->dlogits, dl_tok, dl_perm, st));
   // 4. expert dX chain, second half: dx_perm = dz W13
   a.dz = dz; a.dz_sh = dz_sh; a.dx_perm = dx_perm; a.dx_sh = dx_sh;
   MOE_TRY(run_grouped(BWD1T, a, dims, st));
@@ -644,6 +671,9 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
   const void* x_perm = saved->x_perm;
   if (x_perm == nullptr) {  // selective recompute of the rearranged input
     MOE_LAUNCH(launch_permute_rows(x, saved->dest, *dims, w + L.x_perm_tmp, st));
+    if (cap)
+      MOE_LAUNCH(launch_pad_rows(w + L.x_perm_tmp, dims->d, dims->dtype, offsets_full, dims->E,
+                                 dims->capacity, nullptr, nullptr, st));
     x_perm = w + L.x_perm_tmp;
   }
   a.x_perm = x_perm; a.x = x; a.hw = hw; a.hw_sh = hw_sh;
@@ -652,7 +682,8 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
   MOE_TRY(run_grouped(DW13, a, dims, st));
   // 7. router dW
   if (router)
-    MOE_LAUNCH(launch_dwr(x, saved->row_src, dl_perm, saved->offsets, *dims,
+    MOE_LAUNCH(launch_dwr(x, cap ? row_src_full : saved->row_src, dl_perm,
+                          cap ? offsets_full : saved->offsets, *dims,
                           reinterpret_cast<float*>(w + L.dwr_part), grads->dw_r, st));
   return MOE_OK;
 }

@@ -19,6 +19,11 @@ constexpr int kMaxK = 32;
 
 inline size_t elt_bytes(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 
+// Rows of the permuted buffers: T*k dropless, E*C in the drop-and-pad variant.
+inline int64_t perm_rows(const moe_dims& d) {
+  return d.capacity > 0 ? (int64_t)d.E * d.capacity : d.T * (int64_t)d.k;
+}
+
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
   size_t err;          // int error word (+ padding)
@@ -44,6 +49,9 @@ struct WsLayout {
   size_t x_perm_tmp;   // [T*k, d]   x_perm when the caller does not keep it
   size_t h_tmp;        // [T*k, f]   h when the caller does not keep it
   size_t h_sh_tmp;     // [S*T, f_s]
+  size_t dest_full;    // [T*k] int32   drop-and-pad: dropless position of every copy
+  size_t row_src_full; // [T*k] int32   ... and token of every dropless position
+  size_t offsets_full; // [E+1] int32   ... dropless expert offsets
   size_t total;
   int64_t n_chunks;
   int n_dgate_tiles;
@@ -56,13 +64,24 @@ cudaError_t launch_router_logits(const void* x, const float* w_r, const moe_dims
                                  cudaStream_t st);
 cudaError_t launch_route_topk(const float* logits, const float* bias, int64_t T, int E, int k,
                               int32_t* idx, float* w, int32_t* counts, int num_sms, cudaStream_t st);
+// dgate is gathered from dgate_part at dest (0 for a dropped copy); dl_perm is scattered
+// at dest_dl (the dropless positions, also in the drop-and-pad variant).
 cudaError_t launch_route_bwd(const int32_t* idx, const float* w, const float* dgate_in,
                              const float* dgate_part, int n_part, int64_t part_stride,
-                             const int32_t* dest, int64_t T, int E, int k, float* dgate_out,
-                             float* dlogits, float* dl_tok, float* dl_perm, cudaStream_t st);
+                             const int32_t* dest, const int32_t* dest_dl, int64_t T, int E, int k,
+                             float* dgate_out, float* dlogits, float* dl_tok, float* dl_perm,
+                             cudaStream_t st);
+// With dm.capacity > 0 the permutation is the drop-and-pad one; it also writes the dropless
+// index arrays (dest_full, row_src_full, offsets_full) into the workspace. x == nullptr
+// builds the indices only (no row is moved).
 cudaError_t launch_permute(const void* x, const int32_t* idx, const float* topk_w, const moe_dims& dm,
                            void* x_perm, int32_t* dest, int32_t* row_src, int32_t* offsets,
                            float* w_perm, const WsLayout& L, uint8_t* ws, int* err, cudaStream_t st);
+// Drop-and-pad: zero the padding rows of a [E*C, width] buffer (row i of expert e = i / C is
+// padding when i - e*C >= the expert's dropless count); row_src / w_perm, when given, get
+// -1 / 0 there.
+cudaError_t launch_pad_rows(void* buf, int width, int dtype, const int32_t* offsets_full, int E,
+                            int C, int32_t* row_src, float* w_perm, cudaStream_t st);
 cudaError_t launch_permute_rows(const void* x, const int32_t* dest, const moe_dims& dm, void* x_perm,
                                 cudaStream_t st);
 cudaError_t launch_combine(const void* y_perm, const int32_t* dest, const float* topk_w,

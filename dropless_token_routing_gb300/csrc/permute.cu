@@ -54,8 +54,9 @@ __global__ void __launch_bounds__(kChunk) permute_hist_kernel(
 // then the per-expert totals are scanned into offsets.
 __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __restrict__ chunk_hist,
                                                             int32_t* __restrict__ chunk_base,
-                                                            int64_t n_chunks, int E,
-                                                            int32_t* __restrict__ offsets) {
+                                                            int64_t n_chunks, int E, int capacity,
+                                                            int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ offsets_full) {
   __shared__ int cnt[kMaxE];
   __shared__ int wsum[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -100,8 +101,19 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const int32_t* __res
   }
   __syncthreads();
   const int excl = wsum[warp] + inc - v;
-  if (e < E) offsets[e] = excl;
-  if (e == E - 1) offsets[E] = excl + v;
+  if (capacity > 0) {  // drop-and-pad: uniform segments of C rows; the dropless scan kept aside
+    if (e < E) {
+      offsets[e] = e * capacity;
+      offsets_full[e] = excl;
+    }
+    if (e == E - 1) {
+      offsets[E] = E * capacity;
+      offsets_full[E] = excl + v;
+    }
+  } else {
+    if (e < E) offsets[e] = excl;
+    if (e == E - 1) offsets[E] = excl + v;
+  }
 }
 
 // ---------------------------------------------------------------- P3: scatter + row move
@@ -135,7 +147,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) permute_scatter_kernel(
     const T* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ topk_w,
     const int32_t* __restrict__ local_rank, const int32_t* __restrict__ chunk_base,
-    const int32_t* __restrict__ offsets, int64_t Tn, int d, int k, int64_t n_chunks,
+    const int32_t* __restrict__ offsets, int64_t Tn, int d, int k, int64_t n_chunks, int capacity,
     T* __restrict__ x_perm, int32_t* __restrict__ dest, int32_t* __restrict__ row_src,
     float* __restrict__ w_perm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -146,13 +158,43 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(
       const int r = local_rank[q];
       if (r >= 0) {
         const int e = idx[q];
-        dq = offsets[e] + chunk_base[(int64_t)e * n_chunks + t / kChunk] + r;
-        row_src[dq] = (int32_t)t;
-        if (w_perm != nullptr) w_perm[dq] = topk_w[q];
+        const int rank = chunk_base[(int64_t)e * n_chunks + t / kChunk] + r;  // within expert e
+        // drop-and-pad keeps the first C copies of each expert
+        if (capacity == 0 || rank < capacity) {
+          dq = offsets[e] + rank;
+          row_src[dq] = (int32_t)t;
+          if (w_perm != nullptr) w_perm[dq] = topk_w[q];
+        }
       }
       dest[q] = dq;
     }
-    copy_row_to_dests<T, 4>(x + t * d, x_perm, d, k, dq, lane);
+    if (x != nullptr) copy_row_to_dests<T, 4>(x + t * d, x_perm, d, k, dq, lane);
+  }
+}
+
+// Drop-and-pad: one warp per row of the [E*C, width] buffer; rows past the expert's dropless
+// count are padding and become zero (row_src -1, w_perm 0).
+template <typename T>
+__global__ void __launch_bounds__(256) pad_rows_kernel(T* __restrict__ buf, int width,
+                                                       const int32_t* __restrict__ offsets_full,
+                                                       int E, int C, int32_t* __restrict__ row_src,
+                                                       float* __restrict__ w_perm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int64_t rows = (int64_t)E * C;
+  for (int64_t i = (int64_t)blockIdx.x * nw + warp; i < rows; i += (int64_t)gridDim.x * nw) {
+    const int e = (int)(i / C), r = (int)(i - (int64_t)e * C);
+    if (r < offsets_full[e + 1] - offsets_full[e]) continue;   // a kept copy
+    if (buf != nullptr) {
+      Vec8<T> z;
+      const float zf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      z.from_float(zf);
+      T* row = buf + i * width;
+      for (int v = lane; v < width / 8; v += 32) z.store(row + (int64_t)v * 8);
+    }
+    if (lane == 0) {
+      if (row_src != nullptr) row_src[i] = -1;
+      if (w_perm != nullptr) w_perm[i] = 0.f;
+    }
   }
 }
 
@@ -253,7 +295,8 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, const float* topk_
   if (e != cudaSuccess) return e;
   {
     TraceScope ts(TP_PERMUTE_SCAN, st);
-    permute_scan_kernel<<<1, 1024, 0, st>>>(chunk_hist, chunk_base, L.n_chunks, dm.E, offsets);
+    permute_scan_kernel<<<1, 1024, 0, st>>>(chunk_hist, chunk_base, L.n_chunks, dm.E, dm.capacity,
+                                            offsets, reinterpret_cast<int32_t*>(ws + L.offsets_full));
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -262,11 +305,23 @@ cudaError_t launch_permute(const void* x, const int32_t* idx, const float* topk_
   if (dm.dtype == MOE_F32)
     permute_scatter_kernel<float><<<blocks, 256, 0, st>>>(
         (const float*)x, idx, topk_w, local_rank, chunk_base, offsets, dm.T, dm.d, dm.k, L.n_chunks,
-        (float*)x_perm, dest, row_src, w_perm);
+        dm.capacity, (float*)x_perm, dest, row_src, w_perm);
   else
     permute_scatter_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(
         (const __nv_bfloat16*)x, idx, topk_w, local_rank, chunk_base, offsets, dm.T, dm.d, dm.k,
-        L.n_chunks, (__nv_bfloat16*)x_perm, dest, row_src, w_perm);
+        L.n_chunks, dm.capacity, (__nv_bfloat16*)x_perm, dest, row_src, w_perm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_rows(void* buf, int width, int dtype, const int32_t* offsets_full, int E,
+                            int C, int32_t* row_src, float* w_perm, cudaStream_t st) {
+  const unsigned blocks = (unsigned)token_blocks((int64_t)E * C, 8, 1 << 16);
+  TraceScope ts(TP_MISC, st);
+  if (dtype == MOE_F32)
+    pad_rows_kernel<float><<<blocks, 256, 0, st>>>((float*)buf, width, offsets_full, E, C, row_src, w_perm);
+  else
+    pad_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>((__nv_bfloat16*)buf, width, offsets_full, E, C,
+                                                           row_src, w_perm);
   return cudaGetLastError();
 }
 

@@ -63,6 +63,7 @@ extern "C" int moe_permute_noalloc(const void* x, const int32_t* topk_idx, const
   if (dims->k < 1 || dims->k > kMaxK || (dims->E >= 1 && dims->k > dims->E)) return MOE_ERR_BAD_TOPK;
   if (dims->T < 0 || dims->E < 1 || dims->E > kMaxE || dims->d < 1 || dims->d % 8 != 0)
     return MOE_ERR_BAD_DIMS;
+  if (dims->capacity != 0) return MOE_ERR_BAD_DIMS;   // the dropless permutation only
   const int64_t copies = dims->T * dims->k;
   const int64_t n_chunks = (dims->T + kChunk - 1) / kChunk;
   if (copies > kNoAllocMaxCopies || dims->E * n_chunks > kNoAllocMaxChunkCells)

@@ -150,17 +150,19 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
 __global__ void __launch_bounds__(256) route_bwd_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ w, const float* __restrict__ dgate_in,
     const float* __restrict__ dgate_part, int n_part, int64_t part_stride,
-    const int32_t* __restrict__ dest, int64_t T, int E, int k, float* __restrict__ dgate_out,
-    float* __restrict__ dlogits, float* __restrict__ dl_tok, float* __restrict__ dl_perm) {
+    const int32_t* __restrict__ dest, const int32_t* __restrict__ dest_dl, int64_t T, int E, int k,
+    float* __restrict__ dgate_out, float* __restrict__ dlogits, float* __restrict__ dl_tok,
+    float* __restrict__ dl_perm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < T; t += (int64_t)gridDim.x * nw) {
     const int64_t q = t * k + lane;
     float dg = 0.f, wj = 0.f;
-    int dq = -1, e = -1;
+    int dq = -1, e = -1, dl_at = -1;
     if (lane < k) {
       wj = w[q];
       e = idx[q];
       if (dest != nullptr) dq = dest[q];
+      if (dest_dl != nullptr) dl_at = dest_dl[q];
       if (dgate_in != nullptr) {
         dg = dgate_in[q];
       } else if (dq >= 0) {
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(256) route_bwd_kernel(
     }
     if (lane < k) {
       if (dl_tok != nullptr) dl_tok[q] = dl;
-      if (dl_perm != nullptr && dq >= 0) dl_perm[dq] = dl;
+      if (dl_perm != nullptr && dl_at >= 0) dl_perm[dl_at] = dl;
     }
   }
 }
@@ -476,15 +478,16 @@ cudaError_t launch_route_topk(const float* logits, const float* bias, int64_t T,
 
 cudaError_t launch_route_bwd(const int32_t* idx, const float* w, const float* dgate_in,
                              const float* dgate_part, int n_part, int64_t part_stride,
-                             const int32_t* dest, int64_t T, int E, int k, float* dgate_out,
-                             float* dlogits, float* dl_tok, float* dl_perm, cudaStream_t st) {
+                             const int32_t* dest, const int32_t* dest_dl, int64_t T, int E, int k,
+                             float* dgate_out, float* dlogits, float* dl_tok, float* dl_perm,
+                             cudaStream_t st) {
   const int threads = 256, wpb = threads / 32;
   int64_t blocks = (T + wpb - 1) / wpb;
   if (blocks > 65535) blocks = 65535;
   TraceScope ts(TP_ROUTE_BWD, st);
   route_bwd_kernel<<<(unsigned)blocks, threads, 0, st>>>(idx, w, dgate_in, dgate_part, n_part,
-                                                         part_stride, dest, T, E, k, dgate_out,
-                                                         dlogits, dl_tok, dl_perm);
+                                                         part_stride, dest, dest_dl, T, E, k,
+                                                         dgate_out, dlogits, dl_tok, dl_perm);
   return cudaGetLastError();
 }
 

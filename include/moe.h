@@ -75,6 +75,14 @@ typedef struct moe_dims {
   int32_t S;     /* shared experts (0 allowed) */
   int32_t f_s;   /* shared expert FFN width */
   int32_t dtype; /* enum moe_dtype */
+  /* 0: dropless (every token copy is computed). C > 0: the drop-and-pad variant the pages
+   * compare dropless training with (Pangu Ultra MoE tech-report article, dropless vs
+   * drop-and-pad; CANN MoE page, section 4.3): every expert gets exactly C rows; the first C
+   * copies of an expert in token order are kept, later ones are dropped (dest = -1, they
+   * add nothing to y and pass no gradient back through the expert); unused rows are
+   * zero padding. The permuted buffers (x_perm, row_src, w_perm, z, h, y_perm, dy_perm,
+   * dz, dx_perm) then have R = E*C rows instead of R = T*k, and offsets[e] = e*C. */
+  int32_t capacity;
 } moe_dims;
 
 /* Human-readable text of a status code (static string). */
@@ -115,7 +123,10 @@ int moe_route_topk(const float* logits, const float* bias, int64_t T, int32_t E,
  *   offsets [E+1] int32 (exclusive scan of the per-expert counts),
  *   w_perm [T*k] fp32 or NULL (w_perm[dest[q]] = topk_w[q]).
  * An id outside [0, E) or repeated within a row records MOE_ERR_DEVICE_EXPERT_ID; such copies
- * get dest = -1 and are not moved (nothing is written out of bounds). */
+ * get dest = -1 and are not moved (nothing is written out of bounds).
+ * With dims->capacity = C > 0 (drop-and-pad): x_perm, row_src and w_perm have E*C rows,
+ * offsets[e] = e*C, dest = -1 for a dropped copy, and the padding rows hold zeros
+ * (row_src = -1, w_perm = 0). */
 int moe_permute(const void* x, const int32_t* topk_idx, const float* topk_w, const moe_dims* dims,
                 void* x_perm, int32_t* dest, int32_t* row_src, int32_t* offsets, float* w_perm,
                 void* ws, size_t ws_bytes, moe_stream_t stream);

@@ -50,7 +50,7 @@ import numpy as np
 
 __all__ = [
     "silu", "silu_grad", "router_logits", "selection_scores", "route_topk",
-    "expert_counts", "expert_offsets", "permutation", "swiglu_rows",
+    "expert_counts", "expert_offsets", "permutation", "capacity_permutation", "swiglu_rows",
     "layer_forward", "layer_backward", "router_backward", "as_f64",
     "balance_loss", "balance_loss_grad", "coefficient_of_variation",
 ]
@@ -147,6 +147,35 @@ def permutation(idx, E):
     return dest, row_src
 
 
+def capacity_permutation(idx, E, C):
+    """Drop-and-pad rearrangement with C rows per expert.
+
+    The pages compare dropless training with the drop-and-pad scheme, which gives
+    every expert a fixed number of rows (the Pangu Ultra MoE tech-report article,
+    rjtj.cn, the dropless vs drop-and-pad comparison; the CANN MoE page, gtnt.cn,
+    section 4.3).  Reading taken: the copies of expert e keep the stable order of
+    :func:`permutation`; the first C of them are kept and land in rows
+    ``e*C .. e*C + C - 1``; later copies are dropped (``dest = -1``); rows left over
+    are padding (``row_src = -1``) and hold zeros.
+
+    Returns ``dest [T*k]`` and ``row_src [E*C]``.
+    """
+    idx = np.asarray(idx)
+    T, k = idx.shape
+    flat = idx.reshape(-1)
+    seen = np.zeros(E, np.int64)
+    dest = np.full(T * k, -1, np.int64)
+    row_src = np.full(E * C, -1, np.int64)
+    for q in range(T * k):          # ascending q, as in the dropless order
+        e = flat[q]
+        r = seen[e]
+        seen[e] += 1
+        if r < C:
+            dest[q] = e * C + r
+            row_src[e * C + r] = q // k
+    return dest, row_src
+
+
 def swiglu_rows(X, w13, w2):
     """One expert on a block of rows: returns ``Z = [a | b]``, ``h``, ``Y``.
 
@@ -163,7 +192,7 @@ def swiglu_rows(X, w13, w2):
     return Z, h, Y
 
 
-def layer_forward(x, idx, w, w13, w2, ws13=None, ws2=None):
+def layer_forward(x, idx, w, w13, w2, ws13=None, ws2=None, capacity=0):
     """Dropless MoE forward on fp64 inputs.
 
     ``x [T, d]``, ``idx/w [T, k]`` from :func:`route_topk`, ``w13 [E, 2f, d]``,
@@ -171,25 +200,37 @@ def layer_forward(x, idx, w, w13, w2, ws13=None, ws2=None):
     Returns a dict with ``y`` and every saved intermediate in the permuted
     order (``x_perm``, ``z``, ``h``, ``y_perm``), the shared parts
     (``z_sh[s]``, ``h_sh[s]``, ``y_sh``) and the routing bookkeeping.
+
+    ``capacity = C > 0`` runs the drop-and-pad variant instead
+    (:func:`capacity_permutation`): the permuted buffers have ``E*C`` rows, padding
+    rows are zero, and a dropped copy adds nothing to its token's output (the gates
+    of the kept copies are not renormalised).
     """
     x = np.asarray(x, np.float64)
     T, d = x.shape
     E = w13.shape[0]
     k = idx.shape[1]
     counts = expert_counts(idx, E)
-    offsets = expert_offsets(counts)
-    dest, row_src = permutation(idx, E)
-    x_perm = x[row_src]
+    if capacity > 0:
+        offsets = np.arange(E + 1, dtype=np.int64) * capacity
+        dest, row_src = capacity_permutation(idx, E, capacity)
+    else:
+        offsets = expert_offsets(counts)
+        dest, row_src = permutation(idx, E)
+    R = len(row_src)
+    x_perm = np.zeros((R, d))
+    x_perm[row_src >= 0] = x[row_src[row_src >= 0]]
     f = w13.shape[1] // 2
-    z = np.zeros((T * k, 2 * f))
-    h = np.zeros((T * k, f))
-    y_perm = np.zeros((T * k, d))
+    z = np.zeros((R, 2 * f))
+    h = np.zeros((R, f))
+    y_perm = np.zeros((R, d))
     for e in range(E):
         lo, hi = offsets[e], offsets[e + 1]
         if hi > lo:
             z[lo:hi], h[lo:hi], y_perm[lo:hi] = swiglu_rows(x_perm[lo:hi], w13[e], w2[e])
-    w_perm = np.empty(T * k)
-    w_perm[dest] = np.asarray(w, np.float64).reshape(-1)
+    w_perm = np.zeros(R)
+    kept = dest >= 0
+    w_perm[dest[kept]] = np.asarray(w, np.float64).reshape(-1)[kept]
     y_sh = np.zeros((T, d))
     z_sh, h_sh = [], []
     S = 0 if ws13 is None else ws13.shape[0]
@@ -199,8 +240,10 @@ def layer_forward(x, idx, w, w13, w2, ws13=None, ws2=None):
         h_sh.append(hs)
         y_sh += ys
     y = np.zeros((T, d))
+    dmat = dest.reshape(T, k)
     for j in range(k):
-        y += np.asarray(w, np.float64)[:, j:j + 1] * y_perm[dest.reshape(T, k)[:, j]]
+        on = dmat[:, j] >= 0                  # every copy in the dropless layer
+        y[on] += np.asarray(w, np.float64)[on, j:j + 1] * y_perm[dmat[on, j]]
     y += y_sh
     return dict(y=y, counts=counts, offsets=offsets, dest=dest, row_src=row_src,
                 x_perm=x_perm, z=z, h=h, y_perm=y_perm, w_perm=w_perm,
@@ -235,10 +278,12 @@ def layer_backward(x, idx, w, fwd, dy, w13, w2, ws13=None, ws2=None, w_r=None):
     f = w13.shape[1] // 2
     offsets, dest, row_src = fwd["offsets"], fwd["dest"], fwd["row_src"]
     w_perm = fwd["w_perm"]
-    dy_perm = dy[row_src]
-    dgate_perm = np.zeros(T * k)
-    dz = np.zeros((T * k, 2 * f))
-    dx_perm = np.zeros((T * k, d))
+    R = len(row_src)
+    dy_perm = np.zeros((R, d))
+    dy_perm[row_src >= 0] = dy[row_src[row_src >= 0]]
+    dgate_perm = np.zeros(R)
+    dz = np.zeros((R, 2 * f))
+    dx_perm = np.zeros((R, d))
     dw13 = np.zeros(w13.shape)
     dw2 = np.zeros(w2.shape)
     for e in range(E):
@@ -262,7 +307,8 @@ def layer_backward(x, idx, w, fwd, dy, w13, w2, ws13=None, ws2=None, w_r=None):
     dx = np.zeros((T, d))
     dmat = dest.reshape(T, k)
     for j in range(k):
-        dx += dx_perm[dmat[:, j]]
+        on = dmat[:, j] >= 0                  # a dropped copy passes no gradient back
+        dx[on] += dx_perm[dmat[on, j]]
     S = 0 if ws13 is None else ws13.shape[0]
     dws13 = np.zeros(ws13.shape) if S else None
     dws2 = np.zeros(ws2.shape) if S else None
@@ -277,7 +323,7 @@ def layer_backward(x, idx, w, fwd, dy, w13, w2, ws13=None, ws2=None, w_r=None):
         dx += dzs @ W13
         dws2[s] = dy.T @ hs
         dws13[s] = dzs.T @ x
-    dgate = dgate_perm[dest].reshape(T, k)
+    dgate = np.where(dest >= 0, dgate_perm[np.maximum(dest, 0)], 0.0).reshape(T, k)
     dsel = router_backward(w, dgate)
     dscores = np.zeros((T, E))
     np.put_along_axis(dscores, np.asarray(idx), dsel, axis=1)

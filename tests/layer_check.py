@@ -30,13 +30,13 @@ def _to(t, dev="cuda"):
     return None if t is None else t.to(dev)
 
 
-def run_gpu_layer(w, bwd=True):
+def run_gpu_layer(w, bwd=True, capacity=0):
     from dropless_token_routing_gb300.api import LayerParams, MoELayer, get_device_error
     c = w.cfg
     params = LayerParams(w13=_to(w.w13), w2=_to(w.w2), w_r=_to(w.w_r), bias=_to(w.bias),
                          ws13=_to(w.ws13), ws2=_to(w.ws2))
     layer = MoELayer(params, c["T"], c["d"], c["E"], c["k"], c["f"], c["S"], c["f_s"],
-                     w.torch_dtype, logits_input=w.logits_in is not None)
+                     w.torch_dtype, logits_input=w.logits_in is not None, capacity=capacity)
     x = _to(w.x)
     layer.forward(x, _to(w.logits_in))
     grads = layer.backward(_to(w.dy)) if bwd else None
@@ -45,7 +45,7 @@ def run_gpu_layer(w, bwd=True):
     return layer, grads, err
 
 
-def oracle_layer(w, device_logits=None, bwd=True):
+def oracle_layer(w, device_logits=None, bwd=True, capacity=0):
     """Oracle forward/backward with the top-k taken on the device's fp32 scores."""
     k = w.cfg["k"]
     if w.logits_in is not None:
@@ -56,7 +56,7 @@ def oracle_layer(w, device_logits=None, bwd=True):
     idx, gate = O.route_topk(O.selection_scores(logits32, bias32), k)
     x = O.as_f64(w.x)
     w13, w2, ws13, ws2 = (O.as_f64(t) for t in (w.w13, w.w2, w.ws13, w.ws2))
-    fwd = O.layer_forward(x, idx, gate, w13, w2, ws13, ws2)
+    fwd = O.layer_forward(x, idx, gate, w13, w2, ws13, ws2, capacity=capacity)
     res = dict(idx=idx, gate=gate, fwd=fwd)
     if bwd:
         res["bwd"] = O.layer_backward(x, idx, gate, fwd, O.as_f64(w.dy), w13, w2, ws13, ws2,
@@ -64,10 +64,11 @@ def oracle_layer(w, device_logits=None, bwd=True):
     return res
 
 
-def check_layer(w, bwd=True, report=None):
-    """Run both sides and assert every bar; returns a dict of the measured errors."""
+def check_layer(w, bwd=True, report=None, capacity=0):
+    """Run both sides and assert every bar; returns a dict of the measured errors.
+    capacity = C > 0 checks the drop-and-pad variant against the oracle's."""
     tol = TOL[w.cfg["dtype"]]
-    layer, grads, err = run_gpu_layer(w, bwd=bwd)
+    layer, grads, err = run_gpu_layer(w, bwd=bwd, capacity=capacity)
     assert err == 0, f"device error {err}"
     s = layer.saved
     errs = {}
@@ -75,7 +76,7 @@ def check_layer(w, bwd=True, report=None):
         ref_logits = O.router_logits(O.as_f64(w.x), O.as_f64(w.w_r))
         errs["logits"] = rel(s["logits"], ref_logits)
         assert errs["logits"] <= GATE_TOL, errs
-    ref = oracle_layer(w, device_logits=s["logits"], bwd=bwd)
+    ref = oracle_layer(w, device_logits=s["logits"], bwd=bwd, capacity=capacity)
     fwd = ref["fwd"]
     # bit-exact routing and permutation
     assert np.array_equal(s["topk_idx"].cpu().numpy(), ref["idx"]), "topk_idx differs"
@@ -83,7 +84,10 @@ def check_layer(w, bwd=True, report=None):
     assert np.array_equal(s["offsets"].cpu().numpy(), fwd["offsets"]), "offsets differ"
     assert np.array_equal(s["dest"].cpu().numpy(), fwd["dest"]), "dest differs"
     assert np.array_equal(s["row_src"].cpu().numpy(), fwd["row_src"]), "row_src differs"
-    assert torch.equal(s["x_perm"].cpu(), w.x[torch.as_tensor(fwd["row_src"])]), "x_perm differs"
+    src = torch.as_tensor(fwd["row_src"])
+    xp = torch.zeros(len(src), w.x.shape[1], dtype=w.x.dtype)   # padding rows are zero
+    xp[src >= 0] = w.x[src[src >= 0]]
+    assert torch.equal(s["x_perm"].cpu(), xp), "x_perm differs"
     errs["topk_w"] = rel(s["topk_w"], ref["gate"])
     errs["w_perm"] = rel(s["w_perm"], fwd["w_perm"])
     errs["z"] = rel(s["z"], fwd["z"])

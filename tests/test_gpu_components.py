@@ -102,6 +102,43 @@ def test_permute_matches_stable_counting_sort(T, E, k, skew):
     assert np.linalg.norm(O.as_f64(y) - ref) / np.linalg.norm(ref) <= 5e-3
 
 
+@pytest.mark.parametrize("T,E,k,C", [(1000, 24, 3, 100), (3000, 256, 8, 90), (4097, 64, 6, 1),
+                                     (130, 7, 7, 200)])
+def test_capacity_permute_matches_oracle(T, E, k, C):
+    """Drop-and-pad rearrangement: bit-exact dest / row_src / offsets / w_perm, kept rows
+    moved exactly, padding rows zero."""
+    A = _api()
+    g = torch.Generator().manual_seed(T + E + C)
+    s = torch.randn(T, E, generator=g)
+    s[:, 3] += 2.0                                # one expert overflows
+    idx, _ = O.route_topk(s.numpy(), k)
+    gate = torch.rand(T, k, generator=g)
+    x = torch.randn(T, 64, generator=g).to(torch.bfloat16)
+    dims = A.make_dims(T, 64, E, k, 64, dtype=torch.bfloat16, capacity=C)
+    ws = A.Workspace(dims)
+    R = E * C
+    x_perm = torch.full((R, 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    dest = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    row_src = torch.full((R,), -5, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    w_perm = torch.full((R,), 3.0, dtype=torch.float32, device="cuda")
+    A.permute(x.cuda(), torch.as_tensor(idx, dtype=torch.int32).cuda(), gate.cuda(), dims, x_perm,
+              dest, row_src, offsets, w_perm, ws)
+    assert A.get_device_error(ws) == 0
+    rdest, rsrc = O.capacity_permutation(idx, E, C)
+    assert np.array_equal(dest.cpu().numpy(), rdest)
+    assert np.array_equal(row_src.cpu().numpy(), rsrc)
+    assert np.array_equal(offsets.cpu().numpy(), np.arange(E + 1) * C)
+    src = torch.as_tensor(rsrc)
+    ref = torch.zeros(R, 64, dtype=torch.bfloat16)
+    ref[src >= 0] = x[src[src >= 0]]
+    assert torch.equal(x_perm.cpu(), ref)
+    wp = np.zeros(R, np.float32)
+    kept = rdest >= 0
+    wp[rdest[kept]] = gate.numpy().reshape(-1)[kept]
+    assert np.array_equal(w_perm.cpu().numpy(), wp)
+
+
 def test_permute_rejects_bad_expert_ids_without_writing_out_of_bounds():
     T, E, k = 200, 8, 2
     g = torch.Generator().manual_seed(3)

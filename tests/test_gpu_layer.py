@@ -104,3 +104,42 @@ def test_selective_recompute_gives_identical_results():
     assert torch.equal(y0, y1)
     for k_ in g0:
         assert torch.equal(g0[k_], g1[k_]), k_
+
+
+# ---------------------------------------------------------------- drop-and-pad variant
+@pytest.mark.parametrize("case,cf", [("pangu_small", 1.0), ("pangu_small", 1.25),
+                                     ("adversarial_small", 1.0), ("tiny_fp32", 0.75)])
+def test_capacity_layer_matches_oracle(case, cf):
+    """Drop-and-pad with C = ceil(cf * T * k / E) rows per expert against the oracle's
+    capacity layer: bit-exact dest / row_src / offsets and zero padding rows, the usual
+    float bars on y and every gradient (dropped copies pass nothing back)."""
+    import math
+    from layer_check import check_layer
+    name, over = CASES[case]
+    cfg = shrink(name, **over) if over else dict(__import__("synth").CONFIGS[name], name=name)
+    C = math.ceil(cf * cfg["T"] * cfg["k"] / cfg["E"])
+    layer, grads, _ = check_layer(make_workload(cfg), bwd=True, capacity=C)
+    dest = layer.saved["dest"].cpu()
+    counts = layer.saved["counts"].cpu()
+    assert int((dest >= 0).sum()) == int(torch.clamp(counts, max=C).sum())
+    if case == "adversarial_small":
+        assert (dest < 0).any()        # the hot expert overflows
+
+
+def test_capacity_at_max_count_reproduces_dropless_rows():
+    """With C = the largest expert count nothing is dropped: every row's forward result is
+    the dropless one bit for bit (a row's products do not depend on where it sits), and dx
+    too; the dW products reduce over zero padding rows as well and agree to rounding."""
+    from layer_check import run_gpu_layer
+    w = make_workload(shrink("pangu_bf16", T=640, d=512, E=16, k=4, f=256, f_s=256))
+    ref, gr, e0 = run_gpu_layer(w)
+    C = int(ref.saved["counts"].max().item())
+    cap, gc, e1 = run_gpu_layer(w, capacity=C)
+    assert e0 == 0 and e1 == 0
+    assert (cap.saved["dest"] >= 0).all()
+    assert torch.equal(ref.y, cap.y)
+    assert torch.equal(gr["dx"], gc["dx"])
+    for n in ("dw13", "dw2", "dws13", "dws2"):
+        a, b = gr[n].float(), gc[n].float()
+        assert (torch.linalg.norm(a - b) / torch.linalg.norm(a)).item() <= 2e-3, n
+    assert torch.allclose(gr["dw_r"], gc["dw_r"], rtol=1e-5, atol=1e-6)

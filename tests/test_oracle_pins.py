@@ -354,3 +354,111 @@ def test_balance_loss_gradient_central_differences():
             num[t, e] = (O.balance_loss(sp, counts, k, 0.3)[1] - O.balance_loss(sm, counts, k, 0.3)[1]) / (2 * h)
     assert np.linalg.norm(num - g) / np.linalg.norm(g) < 1e-7
     np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-14)   # softmax Jacobian rows sum to 0
+
+
+# ---------------------------------------------------------------- drop-and-pad pins
+def _kept_brute(idx, C):
+    """Copy (t, j) is kept iff fewer than C copies of its expert come before it in
+    token-major order (pure Python, no sort)."""
+    T, k = len(idx), len(idx[0])
+    kept = [[False] * k for _ in range(T)]
+    for t in range(T):
+        for j in range(k):
+            e = idx[t][j]
+            before = sum(1 for tt in range(T) for jj in range(k)
+                         if (tt, jj) < (t, j) and idx[tt][jj] == e)
+            kept[t][j] = before < C
+    return kept
+
+
+def test_capacity_brute_force_forward():
+    rng = np.random.default_rng(31)
+    T, d, E, k, f, S, f_s = 12, 5, 4, 2, 3, 1, 2
+    x, w_r, w13, w2, ws13, ws2, _ = _rand_layer(rng, T, d, E, k, f, S, f_s)
+    # a skewed router so that some experts overflow a capacity of 3
+    w_r[:, 0] += 2.0 * np.sign(x.mean(0))
+    idx, w = O.route_topk(O.selection_scores(O.router_logits(x, w_r)), k)
+    C = 3
+    assert O.expert_counts(idx, E).max() > C
+    fwd = O.layer_forward(x, idx, w, w13, w2, ws13, ws2, capacity=C)
+    kept = _kept_brute(idx.tolist(), C)
+
+    def ffn(W13, W2, xt):
+        ff = len(W13) // 2
+        a = [sum(W13[i][c] * xt[c] for c in range(d)) for i in range(ff)]
+        b = [sum(W13[ff + i][c] * xt[c] for c in range(d)) for i in range(ff)]
+        hh = [_py_silu(a[i]) * b[i] for i in range(ff)]
+        return [sum(W2[r][i] * hh[i] for i in range(ff)) for r in range(d)]
+
+    for t in range(T):
+        y = [0.0] * d
+        for j in range(k):
+            if kept[t][j]:
+                e = int(idx[t, j])
+                out = ffn(w13[e].tolist(), w2[e].tolist(), x[t].tolist())
+                y = [y[r] + w[t, j] * out[r] for r in range(d)]
+        for s in range(S):
+            out = ffn(ws13[s].tolist(), ws2[s].tolist(), x[t].tolist())
+            y = [y[r] + out[r] for r in range(d)]
+        np.testing.assert_allclose(fwd["y"][t], y, rtol=1e-12, atol=1e-12)
+    # layout: kept copies in rows e*C + rank, padding rows zero and marked -1
+    dest, row_src = fwd["dest"], fwd["row_src"]
+    assert sum(map(sum, kept)) == int(np.sum(dest >= 0))
+    for q in range(T * k):
+        t, j = divmod(q, k)
+        assert (dest[q] >= 0) == kept[t][j]
+        if dest[q] >= 0:
+            assert dest[q] // C == idx[t, j] and row_src[dest[q]] == t
+    pad = row_src < 0
+    assert np.all(fwd["x_perm"][pad] == 0) and np.all(fwd["w_perm"][pad] == 0)
+
+
+def test_capacity_at_least_max_count_equals_dropless():
+    rng = np.random.default_rng(32)
+    T, d, E, k, f = 40, 6, 5, 2, 4
+    x, w_r, w13, w2, _, _, dy = _rand_layer(rng, T, d, E, k, f)
+    idx, w = O.route_topk(O.selection_scores(O.router_logits(x, w_r)), k)
+    C = int(O.expert_counts(idx, E).max())
+    ref = O.layer_forward(x, idx, w, w13, w2)
+    cap = O.layer_forward(x, idx, w, w13, w2, capacity=C)
+    np.testing.assert_allclose(cap["y"], ref["y"], rtol=1e-12, atol=1e-12)
+    assert np.all(cap["dest"] >= 0)
+    # the segment of expert e holds the same rows, shifted from offsets[e] to e*C
+    for e in range(E):
+        lo, hi = ref["offsets"][e], ref["offsets"][e + 1]
+        assert np.array_equal(cap["row_src"][e * C:e * C + hi - lo], ref["row_src"][lo:hi])
+    rb = O.layer_backward(x, idx, w, ref, dy, w13, w2)
+    cb = O.layer_backward(x, idx, w, cap, dy, w13, w2)
+    for name in ("dx", "dw13", "dw2", "dgate", "dscores"):
+        np.testing.assert_allclose(cb[name], rb[name], rtol=1e-11, atol=1e-12)
+
+
+def test_capacity_backward_central_differences():
+    rng = np.random.default_rng(33)
+    T, d, E, k, f, S, f_s = 9, 5, 4, 2, 3, 1, 2
+    C = 3
+    for attempt in range(50):
+        x, w_r, w13, w2, ws13, ws2, dy = _rand_layer(rng, T, d, E, k, f, S, f_s)
+        logits = rng.standard_normal((T, E)) * 2
+        logits[:, 1] += 1.5                  # expert 1 overflows
+        idx0, _ = O.route_topk(O.selection_scores(logits), k)
+        if _margin_ok(logits, k, 1e-3) and O.expert_counts(idx0, E).max() > C:
+            break
+    idx, w = O.route_topk(O.selection_scores(logits), k)
+    fwd = O.layer_forward(x, idx, w, w13, w2, ws13, ws2, capacity=C)
+    assert np.any(fwd["dest"] < 0)
+    bwd = O.layer_backward(x, idx, w, fwd, dy, w13, w2, ws13, ws2)
+
+    def fn():
+        i2, w2_ = O.route_topk(O.selection_scores(logits), k)
+        assert np.array_equal(i2, idx)
+        return float(np.sum(O.layer_forward(x, i2, w2_, w13, w2, ws13, ws2, capacity=C)["y"] * dy))
+
+    for name, arr in [("dx", x), ("dw13", w13), ("dw2", w2), ("dws13", ws13), ("dws2", ws2),
+                      ("dscores", logits)]:
+        num = _fd(fn, arr)
+        ana = bwd[name]
+        rel = np.linalg.norm(num - ana) / np.linalg.norm(ana)
+        assert rel < 1e-6, (name, rel)
+    # a dropped copy has no gate gradient
+    assert np.all(bwd["dgate"].reshape(-1)[fwd["dest"] < 0] == 0)
