@@ -38,9 +38,10 @@ UNIT = "tokens/s"
 # name; valid only while the kernel source still hashes to src_sha256.
 NCU_TRAFFIC = {
     # ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum (one pass)
-    # on the default workload, one launch after warm-up; see profiles/gemm_dw13_pangu_bf16.md
-    "gemm_dw13": {"bytes_per_launch": 2242334208 + 16164291328,
-                  "src_sha256": "6880e5cfbd15c1559669a96146c72968004321ef71382fe550a1ade6470aa634"},
+    # on the default workload, one launch after warm-up; see profiles/gemm_dw13_pangu_bf16.md.
+    # Applies only while the kernel's source file is unchanged since the capture.
+    "gemm_dw13": {"src": "gemm_tc_pair.cu", "bytes_per_launch": 2706356992 + 16168282624,
+                  "src_sha256": "9904b695397a28a2dfe999adf67361af41aefe3cb96e896ff417ca0f35a875eb"},
 }
 
 
@@ -82,6 +83,33 @@ def algorithmic_work(cfg):
         "dwr": Tk * d * es + 8.0 * Tk + 4.0 * 8 * E * d,
     }
     return flops, bytes_
+
+
+def dw_write_bytes(cfg):
+    """Bytes of dW written per launch by the two dW products (bf16 or fp32 gradients)."""
+    es = 4 if cfg["dtype"] == "f32" else 2
+    w13 = 2 * cfg["f"] * cfg["d"] * cfg["E"] + 2 * cfg["f_s"] * cfg["d"] * cfg["S"]
+    return {"gemm_dw13": es * w13, "gemm_dw2": es * w13 // 2}
+
+
+def write_only_bandwidth(device, gib=8, reps=5):
+    """HBM write-only bandwidth (GB/s) of a plain device fill, measured here: the ceiling of
+    kernels whose traffic is almost all writes (the dW products write their whole output
+    and read little)."""
+    import torch
+    buf = torch.empty(gib * 2**30 // 2, dtype=torch.bfloat16, device=device)
+    buf.zero_()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        buf.zero_()
+    b.record()
+    torch.cuda.synchronize()
+    gbs = reps * buf.numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9
+    del buf
+    torch.cuda.empty_cache()
+    return gbs
 
 
 # --------------------------------------------------------------------------- multi-rank
@@ -437,14 +465,18 @@ def main():
                 ent.update(achieved=round(3 * flops[name] / (per_step / 1e3) / 1e12, 1),
                            unit="TFLOP/s (bf16, 3-part weight split, executed)")
         kernels[name] = ent
-    dom = max(trace.items(), key=lambda kv: kv[1][1])[0]
+    # the dominant kernel: the phase with the most time among those with algorithmic work
+    # (the router GEMM aside, whose executed FLOPs are three times its algorithmic ones)
+    ranked = [kv for kv in trace.items() if (kv[0] in flops and kv[0] != "router_gemm") or kv[0] in bytes_]
+    dom = max(ranked or trace.items(), key=lambda kv: kv[1][1])[0]
     dl, dms = trace[dom]
     per = dms / dl
-    src = os.path.join(ROOT, "dropless_token_routing_gb300", "csrc", "gemm_tc.cu")
     traffic = None
     tr = NCU_TRAFFIC.get(dom)
-    if tr and tr.get("src_sha256") == _sha(src):
-        traffic = tr["bytes_per_launch"]
+    if tr and tr.get("bytes_per_launch"):
+        src = os.path.join(ROOT, "dropless_token_routing_gb300", "csrc", tr["src"])
+        if tr.get("src_sha256") == _sha(src):
+            traffic = tr["bytes_per_launch"]
     if dom in flops:
         ach = flops[dom] / (per / 1e3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
@@ -456,6 +488,14 @@ def main():
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm_gbs"], 3), "traffic": traffic, "kernel": dom,
                 "peak_kind": f"HBM copy ({peaks['source']})"}
+    wb = dw_write_bytes(cfg).get(dom)
+    if wb:
+        # the dW products are write streams: their output alone at the write-only ceiling
+        wpk = write_only_bandwidth(dev)
+        wach = wb / (per / 1e3) / 1e9
+        roof["write_stream"] = {"bytes": wb, "achieved": round(wach, 1), "peak": round(wpk, 1),
+                                "unit": "GB/s", "frac": round(wach / wpk, 3),
+                                "peak_kind": "write-only fill bandwidth, measured in this run"}
     gemm_flops = sum(v for k_, v in flops.items() if k_.startswith("gemm"))
     gemm_ms = sum(trace[k_][1] for k_ in trace if k_.startswith("gemm")) / args.steps
     launches = sum(v[0] for v in trace.values())

@@ -1,19 +1,16 @@
 // bf16 grouped expert GEMMs on the 5th-generation tensor cores (sm_103a).
 //
-// One persistent, warp-specialised kernel per matmul kind (see grouped.cuh for the six):
+// One persistent, warp-specialised kernel per matmul kind (the forward, dX-chain and router
+// products of grouped.cuh; the dW products run on CTA pairs, gemm_tc_pair.cu):
 //   warp 0      TMA producer: 4-stage ring of 128x64 A and 256x64 B tiles (128-byte swizzle)
 //   warp 1      TMEM owner and single-thread tcgen05.mma issuer (M=128, N=256, K=16 steps,
 //               fp32 accumulators in TMEM, two accumulator buffers of 256 columns)
 //   warps 2..5  epilogue: tcgen05.ld -> fused math of the mode -> bf16 -> global memory
-//   warp 6      (dW products only) ragged-K fix-up: zeroes the A rows past an expert's
-//               segment in the last K block of a tile, so the producer never blocks on it
 // The tile schedule (groups = routed experts with ragged row counts, then shared experts)
 // is rebuilt by every CTA from the device-resident expert offsets, so nothing waits on the
 // host. Tiles of one expert run N-tile major / M-tile minor so concurrently running CTAs
 // share the expert's weight tile through L2.
-// Ragged edges: M tails read neighbouring rows (or the TMA zero fill) and are not stored;
-// ragged K (the dW products reduce over an expert's rows) zeroes the out-of-segment rows of
-// the A tile in shared memory (warp 6) before the last MMA of the tile.
+// Ragged edges: M tails read neighbouring rows (or the TMA zero fill) and are not stored.
 // Every mbarrier wait is bounded (1 s); on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT,
 // drains its TMA loads and MMAs, frees its TMEM and exits.
 #include <cuda.h>
@@ -32,7 +29,7 @@ constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_STAGE_BYTES = 5120;        // per epilogue warp, a multiple of 1024
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_STAGE_BYTES + 1024;
-constexpr int NUM_THREADS = 224;
+constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int kMaxGroups = 1024 + 8;
 constexpr int SLAB = 64 * 128;                // one 64-element-wide, 64-row swizzled slab
@@ -41,7 +38,6 @@ using namespace tc;
 
 struct TcParams {
   CUtensorMap a0, a1, b0, b1;
-  CUtensorMap o0, o1;  // output maps of the dW products (routed / shared), box {64, 32, 1}
   GroupedArgs g;
 };
 
@@ -77,9 +73,7 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v)
 }
 
 template <int MODE> struct ModeTraits {
-  static constexpr bool a_mn = (MODE == DW2 || MODE == DW13);
-  static constexpr bool b_mn = (MODE == BWD2T || MODE == BWD1T || MODE == DW2 || MODE == DW13);
-  static constexpr bool k_tail = (MODE == DW2 || MODE == DW13);
+  static constexpr bool b_mn = (MODE == BWD2T || MODE == BWD1T);
   static constexpr int bn_eff = (MODE == FWD1) ? BN / 2 : BN;
 };
 
@@ -141,16 +135,6 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
 #pragma unroll
       for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b1, bar, n0 + 64 * i, kl, s);
     }
-  } else {  // DW2 / DW13: A and B both MN-major, K runs over the group's rows
-    const int n0 = tc.ni * BN;
-    const int ka = G.shared ? ((MODE == DW13 ? G.s * T : 0) + k0) : row0 + k0;  // A rows
-    const int kbr = G.shared ? ((MODE == DW2 ? G.s * T : 0) + k0) : row0 + k0;  // B rows
-    const CUtensorMap* am = G.shared ? &p.a1 : &p.a0;
-    const CUtensorMap* bm = G.shared ? &p.b1 : &p.b0;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) tma2d(a_s + i * SLAB, am, bar, m0 + 64 * i, ka);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) tma2d(b_s + i * SLAB, bm, bar, n0 + 64 * i, kbr);
   }
 }
 
@@ -324,54 +308,6 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileCoord
       warp_store_chunk(stage, lane, ph, row_or_null(row_ok, hwr + n0 + c));
     }
     if (!G.shared && row_ok) a.dgate_part[(int64_t)tc.ni * a.dgate_stride + G.row0 + m] = dg;
-  } else if (MODE == DW2 || MODE == DW13) {
-    // dW tiles have no ragged rows: each warp stages its 32 x 64 chunk in the 128-byte
-    // swizzled layout and one lane hands it to the TMA engine (asynchronous tensor store).
-    const int n0 = tc.ni * BN;
-    const int rowc = m0 + (r - lane);          // first row of this warp's 32
-    const CUtensorMap* om = G.shared ? &p.o1 : &p.o0;
-    const int zc = G.shared ? G.s : G.e;
-    const bool empty = G.K == 0;               // dW of an expert without rows
-    if (rowc < G.M) {
-      const int nch = (min(BN, G.N - n0) + 63) / 64;
-      // software pipeline: the TMEM load of chunk c+1 is in flight while chunk c is staged
-      uint32_t u[64];
-      if (!empty) {
-        tmem_ld32(acc, *reinterpret_cast<uint32_t(*)[32]>(u));
-        tmem_ld32(acc + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
-      }
-#pragma unroll 1
-      for (int ch = 0; ch < nch; ++ch) {
-        const int c = ch * 64;
-        if (!empty) {
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            pk[q] = make_uint4(pack_bf16x2(__uint_as_float(u[8 * q]), __uint_as_float(u[8 * q + 1])),
-                               pack_bf16x2(__uint_as_float(u[8 * q + 2]), __uint_as_float(u[8 * q + 3])),
-                               pack_bf16x2(__uint_as_float(u[8 * q + 4]), __uint_as_float(u[8 * q + 5])),
-                               pack_bf16x2(__uint_as_float(u[8 * q + 6]), __uint_as_float(u[8 * q + 7])));
-          if (ch + 1 < nch) {
-            tmem_ld32(acc + c + 64, *reinterpret_cast<uint32_t(*)[32]>(u));
-            tmem_ld32(acc + c + 96, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
-          }
-        } else {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) pk[q] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (lane == 0) bulk_wait_read0();      // the previous store has left the buffer
-        __syncwarp();
-        uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) srow[q ^ (lane & 7)] = pk[q];
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          tma_store3d(om, smem_u32(stage), n0 + c, rowc, zc);
-          bulk_commit();
-        }
-      }
-    }
   } else {  // FWD2 / BWD1T: rows of ragged expert segments, stored row by row
     const int n0 = tc.ni * BN;
     __nv_bfloat16* out;
@@ -398,7 +334,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
   using TR = ModeTraits<MODE>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
-  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], tail_bar[STAGES], final_bar;
+  __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], final_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
   __shared__ int tile_start[kMaxGroups + 1];
@@ -420,7 +356,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
       mbar_init(smem_u32(&tfull_bar[b]), 1);
       mbar_init(smem_u32(&tempty_bar[b]), 4);
     }
-    for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&tail_bar[s]), 1);
     mbar_init(smem_u32(&final_bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -445,8 +380,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     uint32_t phase = 0;
     uint32_t pending = 0;    // stages whose latest load may still be in flight
     uint32_t pend_par = 0;   // parity of the phase that load completes, per stage
-    uint32_t pend_tail = 0;  // ... and whether it completes on tail_bar (else full_bar)
-    uint32_t tail_par = 0;   // next tail_bar parity, per stage
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM, s_off);
@@ -456,62 +389,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
                                            a.err, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
-        const bool tail = TR::k_tail && tc.G.K - kb * BK < BK;
-        // a ragged last K block lands on tail_bar; warp 6 zeroes it and then completes full_bar
-        const uint32_t bar = tail ? smem_u32(&tail_bar[stage]) : smem_u32(&full_bar[stage]);
+        const uint32_t bar = smem_u32(&full_bar[stage]);
         if (lane == 0) {
           mbar_arrive_expect_tx(bar, STAGE_BYTES);
           issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, bar);
         }
-        const uint32_t par = tail ? (tail_par >> stage) & 1u : phase;
         pending |= 1u << stage;
-        pend_par = (pend_par & ~(1u << stage)) | (par << stage);
-        pend_tail = (pend_tail & ~(1u << stage)) | ((tail ? 1u : 0u) << stage);
-        if (tail) tail_par ^= 1u << stage;
+        pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
     // drain: no TMA load may still be writing shared memory when the CTA exits
     for (int s = 0; s < STAGES; ++s)
       if ((pending >> s) & 1u)
-        mbar_wait_bounded(smem_u32((pend_tail >> s) & 1u ? &tail_bar[s] : &full_bar[s]),
-                          (pend_par >> s) & 1u, nullptr, a.err, kWaitLimitNs);
-  } else if (warp == 6) {
-    // ------------------------------------------------------------ ragged-K fix-up (dW only)
-    if (TR::k_tail) {
-      int stage = 0;
-      uint32_t tail_par = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM, s_off);
-        const int nkb = (tc.G.K + BK - 1) / BK;
-        for (int kb = 0; kb < nkb; ++kb) {
-          const int rem = tc.G.K - kb * BK;
-          if (rem < BK) {
-            const bool got = mbar_wait_bounded(smem_u32(&tail_bar[stage]), (tail_par >> stage) & 1u,
-                                               &abort_flag, a.err, kWaitLimitNs);
-            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-            tail_par ^= 1u << stage;
-            // zero K rows [rem, roundup16(rem)) of both 64-wide slabs of the MN-major A tile;
-            // the MMA issuer stops at roundup16(rem), so rows past that are never read
-            uint4* A4 = reinterpret_cast<uint4*>(smem + stage * STAGE_BYTES);
-            const int per_slab = (((rem + 15) & ~15) - rem) * 8;  // 16-byte chunks
-            for (int i = lane; i < 2 * per_slab; i += 32) {
-              const int sl = i / per_slab, j = i - sl * per_slab;
-              A4[sl * (SLAB / 16) + rem * 8 + j] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&full_bar[stage]));
-          }
-          if (++stage == STAGES) stage = 0;
-        }
-      }
-    }
+        mbar_wait_bounded(smem_u32(&full_bar[s]), (pend_par >> s) & 1u, nullptr, a.err, kWaitLimitNs);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (one thread)
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN, TR::a_mn, TR::b_mn);
+      constexpr uint32_t idesc = idesc_bf16(BM, BN, false, TR::b_mn);
       int stage = 0;
       uint32_t phase = 0;
       bool issued = false, ok = true;
@@ -529,12 +424,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
                                  kWaitLimitNs)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
-          // K=16 steps in this block: 4, or fewer in a ragged last block of a dW product
-          const int nks = TR::k_tail ? min(BK, tc.G.K - kb * BK + 15) / 16 : BK / 16;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            if (kk >= nks) break;
-            const uint64_t ad = TR::a_mn ? sdesc(a_s + kk * 2048, SLAB, 1024) : sdesc(a_s + kk * 32, 16, 1024);
+            const uint64_t ad = sdesc(a_s + kk * 32, 16, 1024);
             const uint64_t bd = TR::b_mn ? sdesc(b_s + kk * 2048, SLAB, 1024) : sdesc(b_s + kk * 32, 16, 1024);
             umma(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
@@ -552,7 +444,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
       }
     }
     __syncwarp();
-  } else if (warp >= 2 && warp <= 5) {
+  } else {
     // ------------------------------------------------------------ epilogue warps 2..5
     const int lg = warp & 3;              // TMEM lane quarter this warp may access
     const int r = lg * 32 + lane;         // tile row
@@ -571,7 +463,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[b]));
     }
-    if (lane == 0) bulk_wait0();  // tensor stores of the dW products fully written
   }
   __syncthreads();
   if (warp == 1) {
@@ -586,7 +477,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
 
 constexpr int trace_phase_of(int mode) {
   return mode == FWD1 ? TP_GEMM_FWD1 : mode == FWD2 ? TP_GEMM_FWD2 : mode == BWD2T ? TP_GEMM_BWD2T
-       : mode == BWD1T ? TP_GEMM_BWD1T : mode == DW2 ? TP_GEMM_DW2 : mode == DW13 ? TP_GEMM_DW13
+       : mode == BWD1T ? TP_GEMM_BWD1T
        : TP_ROUTER_GEMM;
 }
 
@@ -609,6 +500,7 @@ int launch_mode(TcParams& p, int num_sms, cudaStream_t st) {
 int tc_dgate_tiles(int f) { return (f + BN - 1) / BN; }
 
 int launch_tc_grouped(int mode, const GroupedArgs& g, int num_sms, cudaStream_t st) {
+  if (mode == DW2 || mode == DW13) return launch_tc_pair_dw(mode, g, num_sms, st);
   TcParams p;
   memset(&p, 0, sizeof(p));
   p.g = g;
@@ -641,20 +533,8 @@ int launch_tc_grouped(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
       ok = map2d(&p.a0, g.x, d, T, 64, 128) && map2d(&p.b0, g.w_split, 3 * d, E, 64, 256);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<ROUTER>(p, num_sms, st);
-    case DW2:
-      ok = map2d(&p.a0, g.dy_perm, d, Tk, 64, 64) && map2d(&p.b0, g.hw, f, Tk, 64, 64) &&
-           map3d(&p.o0, g.dw2, f, d, E, 64, 32);
-      if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 64) && map2d(&p.b1, g.hw_sh, fs, ST, 64, 64) &&
-                   map3d(&p.o1, g.dws2, fs, d, S, 64, 32);
-      if (!ok) return MOE_ERR_CUDA;
-      return launch_mode<DW2>(p, num_sms, st);
     default:
-      ok = map2d(&p.a0, g.dz, 2 * f, Tk, 64, 64) && map2d(&p.b0, g.x_perm, d, Tk, 64, 64) &&
-           map3d(&p.o0, g.dw13, d, 2 * f, E, 64, 32);
-      if (sh) ok = ok && map2d(&p.a1, g.dz_sh, 2 * fs, ST, 64, 64) && map2d(&p.b1, g.x, d, T, 64, 64) &&
-                   map3d(&p.o1, g.dws13, d, 2 * fs, S, 64, 32);
-      if (!ok) return MOE_ERR_CUDA;
-      return launch_mode<DW13>(p, num_sms, st);
+      return MOE_ERR_BAD_DIMS;
   }
 }
 

@@ -107,5 +107,7 @@ int tc_dgate_tiles(int f);
 cudaError_t launch_simt_grouped(int mode, const GroupedArgs& a, int num_sms, cudaStream_t st);
 // Returns MOE_OK or a negative status (tensor-map encoding can fail on the host).
 int launch_tc_grouped(int mode, const GroupedArgs& a, int num_sms, cudaStream_t st);
+// dW2 / dW13 on CTA pairs (tcgen05.mma.cta_group::2)
+int launch_tc_pair_dw(int mode, const GroupedArgs& a, int num_sms, cudaStream_t st);
 
 }  // namespace moe
