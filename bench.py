@@ -228,46 +228,61 @@ def cpu_baseline(w, logits32, n_tokens):
                       f"({n_exp} routed experts they use + shared, full d/f), {dt:.1f} s"}
 
 
-# --------------------------------------------------------------------------- drop-and-pad
+# --------------------------------------------------------------------------- layer variants
+def time_variant(params, cfg, w, args, stream, **kw):
+    """ms per fwd+bwd step of a layer variant (MoELayer keyword arguments), timed like the
+    main step on the same workload, this rank only."""
+    import torch
+    from dropless_token_routing_gb300.api import MoELayer, get_device_error
+    T, k, E = cfg["T"], cfg["k"], cfg["E"]
+    lay = MoELayer(params, T, cfg["d"], E, k, cfg["f"], cfg["S"], cfg["f_s"], w.torch_dtype,
+                   device=w.x.device, logits_input=w.logits_in is not None, **kw)
+    lay.alloc_grads()
+
+    def step():
+        lay.forward(w.x, w.logits_in)
+        lay.backward(w.dy)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if get_device_error(lay.ws) != 0:
+        raise RuntimeError(f"device error in the {kw} run")
+    ms = a.elapsed_time(b) / args.steps
+    del lay
+    torch.cuda.empty_cache()
+    return ms
+
+
 def drop_and_pad(factors, params, cfg, w, counts, args, stream):
     """The comparison the pages draw: the same layer step in the drop-and-pad variant, every
     expert given C = ceil(cf * T * k / E) rows (overflow copies dropped, short experts
-    padded). Timed like the dropless step, same workload, on this rank only."""
+    padded)."""
     import math
-    import torch
-    from dropless_token_routing_gb300.api import MoELayer, get_device_error
     T, k, E = cfg["T"], cfg["k"], cfg["E"]
     out = []
     for cf in factors:
         C = max(1, math.ceil(cf * T * k / E))
-        lay = MoELayer(params, T, cfg["d"], E, k, cfg["f"], cfg["S"], cfg["f_s"], w.torch_dtype,
-                       device=w.x.device, logits_input=w.logits_in is not None, capacity=C)
-        lay.alloc_grads()
-
-        def step():
-            lay.forward(w.x, w.logits_in)
-            lay.backward(w.dy)
-
-        for _ in range(args.warmup):
-            step()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
-            step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        if get_device_error(lay.ws) != 0:
-            raise RuntimeError("device error in the drop-and-pad run")
-        ms = a.elapsed_time(b) / args.steps
+        ms = time_variant(params, cfg, w, args, stream, capacity=C)
         kept = sum(min(c, C) for c in counts)
         out.append({"capacity_factor": cf, "capacity": C, "value": round(T / (ms / 1e3), 1),
                     "unit": UNIT, "ms_per_step": round(ms, 3),
                     "dropped_copy_fraction": round(1 - kept / (T * k), 4),
                     "padding_row_fraction": round(1 - kept / (E * C), 4)})
-        del lay
-        torch.cuda.empty_cache()
     return out
+
+
+def fused_rearrange(params, cfg, w, args, stream):
+    """The rearrangement fused into the expert GEMMs' operand loads (TMA row gathers from x
+    and dy, no rearranged copies) instead of the copies the default step makes."""
+    ms = time_variant(params, cfg, w, args, stream, rearrange=1, recompute=True)
+    return {"value": round(cfg["T"] / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3)}
 
 
 # --------------------------------------------------------------------------- main
@@ -282,6 +297,9 @@ def main():
     ap.add_argument("--oracle-tokens", type=int, default=4)
     ap.add_argument("--shrink", default="", help="smaller case of the same recipe, e.g. T=512,E=16 "
                                                   "(for profiler captures; not a bench line)")
+    ap.add_argument("--no-fused-rearrange", dest="fused_rearrange", action="store_false",
+                    help="skip the timing of the fused-rearrangement variant (rank 0, after the "
+                         "main measurement)")
     ap.add_argument("--drop-pad", default="1.0,1.25",
                     help="capacity factors of the drop-and-pad comparison runs (rank 0, after the "
                          "dropless measurement; empty to skip)")
@@ -393,34 +411,66 @@ def main():
     value = throughput(world, args.steps, T, t_ms)
 
     # ---------------------------------------------------------------- end to end
+    # Every step copies its inputs from pinned host memory and reads y and dx back. The copies
+    # run on a second stream, double-buffered: step i+2's inputs land while step i computes,
+    # y is read back during the backward and dx during the next forward.
     h_x = x.cpu().pin_memory()
     h_dy = dy.cpu().pin_memory()
     h_li = li.cpu().pin_memory() if li is not None else None
     h_y = torch.empty_like(h_x).pin_memory()
     h_dx = torch.empty_like(h_x).pin_memory()
-    d_x, d_dy = torch.empty_like(x), torch.empty_like(dy)
-    d_li = torch.empty_like(li) if li is not None else None
+    copy = torch.cuda.Stream(device=dev)
+    d_in = [(torch.empty_like(x), torch.empty_like(dy), torch.empty_like(li) if li is not None else None)
+            for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # the slot's inputs have landed
+    ev_used = [torch.cuda.Event() for _ in range(2)]   # the compute is done with the slot
+    ev_y, ev_yd, ev_dx, ev_dxd = (torch.cuda.Event() for _ in range(4))
 
-    def e2e_step():
-        d_x.copy_(h_x, non_blocking=True)
-        d_dy.copy_(h_dy, non_blocking=True)
-        if d_li is not None:
-            d_li.copy_(h_li, non_blocking=True)
-        y = layer.forward(d_x, d_li)
-        h_y.copy_(y, non_blocking=True)
-        g = layer.backward(d_dy)
-        h_dx.copy_(g["dx"], non_blocking=True)
+    def h2d(slot):
+        with torch.cuda.stream(copy):
+            copy.wait_event(ev_used[slot])
+            bx, bdy, bli = d_in[slot]
+            bx.copy_(h_x, non_blocking=True)
+            bdy.copy_(h_dy, non_blocking=True)
+            if bli is not None:
+                bli.copy_(h_li, non_blocking=True)
+            ev_in[slot].record(copy)
 
-    for _ in range(2):
-        e2e_step()
+    def e2e_run(n):
+        copy.wait_stream(stream)
+        for s_ in range(min(2, n)):
+            h2d(s_)
+        for i in range(n):
+            s_ = i % 2
+            bx, bdy, bli = d_in[s_]
+            stream.wait_event(ev_in[s_])
+            stream.wait_event(ev_yd)          # the previous y has been read back
+            y = layer.forward(bx, bli)
+            ev_y.record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev_y)
+                h_y.copy_(y, non_blocking=True)
+                ev_yd.record(copy)
+            stream.wait_event(ev_dxd)         # the previous dx has been read back
+            g = layer.backward(bdy)
+            ev_used[s_].record(stream)
+            ev_dx.record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev_dx)
+                h_dx.copy_(g["dx"], non_blocking=True)
+                ev_dxd.record(copy)
+            if i + 2 < n:
+                h2d(s_)                       # the inputs of step i + 2
+        stream.wait_stream(copy)
+
+    e2e_run(2)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     k_e2e = max(3, args.steps // 2)
     e2.record(stream)
-    for _ in range(k_e2e):
-        e2e_step()
+    e2e_run(k_e2e)
     e3.record(stream)
     torch.cuda.synchronize()
     t_e2e = reduce_max(e2.elapsed_time(e3), dev)
@@ -520,6 +570,8 @@ def main():
     factors = [float(v) for v in args.drop_pad.split(",") if v.strip()]
     if factors:
         line["drop_and_pad"] = drop_and_pad(factors, params, cfg, w, cnt, args, stream)
+    if args.fused_rearrange and cfg["dtype"] == "bf16":
+        line["fused_rearrange"] = fused_rearrange(params, cfg, w, args, stream)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

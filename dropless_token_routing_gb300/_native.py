@@ -40,7 +40,8 @@ class MoeError(RuntimeError):
 
 class MoeDims(ctypes.Structure):
     _fields_ = [("T", c_int64), ("d", c_int32), ("E", c_int32), ("k", c_int32), ("f", c_int32),
-                ("S", c_int32), ("f_s", c_int32), ("dtype", c_int32), ("capacity", c_int32)]
+                ("S", c_int32), ("f_s", c_int32), ("dtype", c_int32), ("capacity", c_int32),
+                ("rearrange", c_int32)]
 
 
 class LayerParams(ctypes.Structure):

@@ -31,10 +31,11 @@ def _dt(dtype) -> int:
     raise ValueError(f"unsupported dtype {dtype}")
 
 
-def make_dims(T, d, E, k, f, S=0, f_s=0, dtype=torch.bfloat16, capacity=0) -> N.MoeDims:
-    """capacity = 0: dropless; C > 0: drop-and-pad with C rows per expert."""
+def make_dims(T, d, E, k, f, S=0, f_s=0, dtype=torch.bfloat16, capacity=0, rearrange=0) -> N.MoeDims:
+    """capacity = 0: dropless; C > 0: drop-and-pad with C rows per expert.
+    rearrange = 0: rearranged copies; 1: rearrangement fused into the GEMM loads."""
     return N.MoeDims(int(T), int(d), int(E), int(k), int(f), int(S), int(f_s) if S else 0, _dt(dtype),
-                     int(capacity))
+                     int(capacity), int(rearrange))
 
 
 def perm_rows(dims: N.MoeDims) -> int:
@@ -161,13 +162,14 @@ class MoELayer:
     ``forward(x, logits_in=None)`` runs moe_layer_fwd; ``backward(dy)`` runs
     moe_layer_bwd on the values the last forward saved. ``recompute=True`` keeps neither
     the rearranged input nor h between the two (selective recompute). ``capacity=C > 0``
-    runs the drop-and-pad variant with C rows per expert instead of the dropless layer.
+    runs the drop-and-pad variant with C rows per expert instead of the dropless layer;
+    ``rearrange=1`` fuses the rearrangement into the GEMMs' operand loads.
     """
 
     def __init__(self, params: LayerParams, T, d, E, k, f, S=0, f_s=0, dtype=torch.bfloat16,
-                 device="cuda", logits_input=False, recompute=False, capacity=0):
+                 device="cuda", logits_input=False, recompute=False, capacity=0, rearrange=0):
         self.params = params
-        self.dims = make_dims(T, d, E, k, f, S, f_s, dtype, capacity)
+        self.dims = make_dims(T, d, E, k, f, S, f_s, dtype, capacity, rearrange)
         self.T, self.d, self.E, self.k, self.f, self.S, self.f_s = T, d, E, k, f, S, f_s
         self.dtype = dtype
         Tk = T * k

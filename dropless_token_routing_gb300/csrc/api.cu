@@ -112,6 +112,7 @@ int check_dims(const moe_dims* d) {
   const int unit = d->dtype == MOE_BF16 ? 64 : 8;
   if (d->d % unit != 0 || d->f % unit != 0 || (d->S > 0 && d->f_s % unit != 0)) return MOE_ERR_BAD_DIMS;
   if (d->capacity < 0 || (int64_t)d->capacity * d->E >= (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
+  if (d->rearrange != MOE_REARRANGE_COPY && d->rearrange != MOE_REARRANGE_GATHER) return MOE_ERR_BAD_DIMS;
   const int64_t rows = d->T * (int64_t)d->k + perm_rows(*d) + (int64_t)d->S * d->T;
   if (d->T > (int64_t)0x7fffffff || rows >= (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
   return MOE_OK;
@@ -184,6 +185,14 @@ int run_router(const void* x, const float* w_r, const moe_dims* d, float* logits
   MOE_TRY(launch_tc_grouped(ROUTER, a, dev_info().sms, st));
   return launch_router_reduce(part, d->T, d->E, kRouterSplit, logits, st) == cudaSuccess ? MOE_OK
                                                                                         : MOE_ERR_LAUNCH;
+}
+
+// MOE_REARRANGE_GATHER on the bf16 dropless path fuses the rearrangement into the expert
+// GEMMs: their routed token operands are gathered from x / dy by row_src (TMA row gathers),
+// so x_perm and dy_perm are never materialised. fp32 (SIMT kernels) and drop-and-pad (zero
+// padding rows) always keep the rearranged copies.
+bool fused_gather(const moe_dims* d) {
+  return d->rearrange == MOE_REARRANGE_GATHER && d->dtype == MOE_BF16 && d->capacity == 0;
 }
 
 int dgate_tiles(const moe_dims* d) {
@@ -531,7 +540,9 @@ int moe_layer_fwd(const moe_layer_params* params, const void* x, const float* lo
   const cudaStream_t st = (cudaStream_t)stream;
   const WsLayout L = ws_layout(*dims);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  void* x_perm = saved->x_perm != nullptr ? saved->x_perm : (void*)(w + L.x_perm_tmp);
+  const bool gather = fused_gather(dims);
+  // with the fused gather x_perm is written only when the caller keeps it
+  void* x_perm = saved->x_perm != nullptr ? saved->x_perm : gather ? nullptr : (void*)(w + L.x_perm_tmp);
   void* h = saved->h != nullptr ? saved->h : (void*)(w + L.h_tmp);
   void* h_sh = dims->S == 0 ? nullptr : saved->h_sh != nullptr ? saved->h_sh : (void*)(w + L.h_sh_tmp);
   if (dims->T == 0) {
@@ -548,14 +559,15 @@ int moe_layer_fwd(const moe_layer_params* params, const void* x, const float* lo
   if (cudaMemsetAsync(saved->counts, 0, sizeof(int32_t) * dims->E, st) != cudaSuccess) return MOE_ERR_CUDA;
   MOE_LAUNCH(launch_route_topk(scores, params->bias, dims->T, dims->E, dims->k, saved->topk_idx,
                                saved->topk_w, saved->counts, dev_info().sms, st));
-  MOE_LAUNCH(launch_permute(x, saved->topk_idx, saved->topk_w, *dims, x_perm, saved->dest,
-                            saved->row_src, saved->offsets, saved->w_perm, L, w,
+  MOE_LAUNCH(launch_permute(x_perm != nullptr ? x : nullptr, saved->topk_idx, saved->topk_w, *dims, x_perm,
+                            saved->dest, saved->row_src, saved->offsets, saved->w_perm, L, w,
                             reinterpret_cast<int*>(w + L.err), st));
   if (dims->capacity > 0)
     MOE_LAUNCH(launch_pad_rows(x_perm, dims->d, dims->dtype, reinterpret_cast<int32_t*>(w + L.offsets_full),
                                dims->E, dims->capacity, saved->row_src, saved->w_perm, st));
   GroupedArgs a = base_args(dims, saved->offsets, reinterpret_cast<int*>(w + L.err));
   a.x_perm = x_perm; a.x = x; a.w13 = params->w13; a.w2 = params->w2;
+  a.gather_rows = gather ? saved->row_src : nullptr;
   a.ws13 = params->ws13; a.ws2 = params->ws2;
   a.z_out = saved->z; a.h_out = h; a.z_sh_out = saved->z_sh; a.h_sh_out = h_sh;
   MOE_TRY(run_grouped(FWD1, a, dims, st));
@@ -639,13 +651,17 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
     MOE_LAUNCH(launch_permute(nullptr, saved->topk_idx, nullptr, full, nullptr, dest_full, row_src_full,
                               offsets_full, nullptr, L, w, err, st));
   }
-  // 1. rearrange dY like x
-  MOE_LAUNCH(launch_permute_rows(dy, saved->dest, *dims, dy_perm, st));
-  if (cap)
-    MOE_LAUNCH(launch_pad_rows(dy_perm, dims->d, dims->dtype, offsets_full, dims->E, dims->capacity,
-                               nullptr, nullptr, st));
+  // 1. rearrange dY like x (fused into the GEMMs' operand loads on the bf16 dropless path)
+  const bool gather = fused_gather(dims);
+  if (!gather) {
+    MOE_LAUNCH(launch_permute_rows(dy, saved->dest, *dims, dy_perm, st));
+    if (cap)
+      MOE_LAUNCH(launch_pad_rows(dy_perm, dims->d, dims->dtype, offsets_full, dims->E, dims->capacity,
+                                 nullptr, nullptr, st));
+  }
   // 2. expert dX chain, first half: D = dY W2, dgate partials, dz, hw
   GroupedArgs a = base_args(dims, saved->offsets, err);
+  a.gather_rows = gather ? saved->row_src : nullptr;
   a.dy_perm = dy_perm; a.dy = dy; a.z = saved->z; a.z_sh = saved->z_sh;
   a.w13 = params->w13; a.w2 = params->w2; a.ws13 = params->ws13; a.ws2 = params->ws2;
   a.w_perm = saved->w_perm;
@@ -669,7 +685,7 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
                             grads->dx, st));
   // 6. expert dW products (separate kernels from the dX chain)
   const void* x_perm = saved->x_perm;
-  if (x_perm == nullptr) {  // selective recompute of the rearranged input
+  if (x_perm == nullptr && !gather) {  // selective recompute of the rearranged input
     MOE_LAUNCH(launch_permute_rows(x, saved->dest, *dims, w + L.x_perm_tmp, st));
     if (cap)
       MOE_LAUNCH(launch_pad_rows(w + L.x_perm_tmp, dims->d, dims->dtype, offsets_full, dims->E,

@@ -38,6 +38,7 @@ using namespace tc;
 
 struct TcParams {
   CUtensorMap a0, a1, b0, b1;
+  CUtensorMap g0;      // row gather of the routed A operand (x or dy, box {64, 1})
   GroupedArgs g;
 };
 
@@ -78,9 +79,11 @@ template <int MODE> struct ModeTraits {
 };
 
 // ------------------------------------------------------------------ producer: TMA issue
+// `gather`: the routed A tile is gathered row by row by the whole producer warp instead
+// (issue_gather_a), so it is skipped here.
 template <int MODE>
 __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCoord& tc, int kb,
-                                                 uint32_t a_s, uint32_t b_s, uint32_t bar) {
+                                                 uint32_t a_s, uint32_t b_s, uint32_t bar, bool gather) {
   const GroupedArgs& a = p.g;
   const GroupGeom& G = tc.G;
   const int m0 = tc.mi * BM;
@@ -94,7 +97,7 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
   } else if (MODE == FWD1) {
     const int j0 = tc.ni * (BN / 2);
     if (!G.shared) {
-      tma2d(a_s, &p.a0, bar, k0, row0 + m0);
+      if (!gather) tma2d(a_s, &p.a0, bar, k0, row0 + m0);
       tma3d(b_s, &p.b0, bar, k0, j0, G.e);
       tma3d(b_s + B_BYTES / 2, &p.b0, bar, k0, a.f + j0, G.e);
     } else {
@@ -115,7 +118,7 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
   } else if (MODE == BWD2T) {
     const int n0 = tc.ni * BN;
     if (!G.shared) {
-      tma2d(a_s, &p.a0, bar, k0, row0 + m0);
+      if (!gather) tma2d(a_s, &p.a0, bar, k0, row0 + m0);
 #pragma unroll
       for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b0, bar, n0 + 64 * i, k0, G.e);
     } else {
@@ -384,6 +387,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM, s_off);
       const int nkb = (tc.G.K + BK - 1) / BK;
+      // fused rearrangement: lane j gathers tile rows 4j..4j+3 (rows past the segment repeat
+      // its first row; they are computed but never stored)
+      const bool gather = (MODE == FWD1 || MODE == BWD2T) && a.gather_rows != nullptr && !tc.G.shared;
+      int tok[4] = {0, 0, 0, 0};
+      if (gather) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int m = tc.mi * BM + 4 * lane + i;
+          tok[i] = __ldg(a.gather_rows + tc.G.row0 + (m < tc.G.M ? m : 0));
+        }
+      }
       for (int kb = 0; kb < nkb; ++kb) {
         const bool got = mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, &abort_flag,
                                            a.err, kWaitLimitNs);
@@ -392,7 +406,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
         const uint32_t bar = smem_u32(&full_bar[stage]);
         if (lane == 0) {
           mbar_arrive_expect_tx(bar, STAGE_BYTES);
-          issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, bar);
+          issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, bar, gather);
+        }
+        if (gather) {
+          __syncwarp();
+          tma_gather4(a_s + 512 * lane, &p.g0, bar, kb * BK, tok[0], tok[1], tok[2], tok[3]);
         }
         pending |= 1u << stage;
         pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
@@ -510,7 +528,8 @@ int launch_tc_grouped(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
   const bool sh = g.S > 0;
   switch (mode) {
     case FWD1:
-      ok = map2d(&p.a0, g.x_perm, d, Tk, 64, 128) && map3d(&p.b0, g.w13, d, 2 * f, E, 64, 128);
+      ok = (g.gather_rows != nullptr ? map2d(&p.g0, g.x, d, T, 64, 1) : map2d(&p.a0, g.x_perm, d, Tk, 64, 128)) &&
+           map3d(&p.b0, g.w13, d, 2 * f, E, 64, 128);
       if (sh) ok = ok && map2d(&p.a1, g.x, d, T, 64, 128) && map3d(&p.b1, g.ws13, d, 2 * fs, S, 64, 128);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<FWD1>(p, num_sms, st);
@@ -520,7 +539,8 @@ int launch_tc_grouped(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<FWD2>(p, num_sms, st);
     case BWD2T:
-      ok = map2d(&p.a0, g.dy_perm, d, Tk, 64, 128) && map3d(&p.b0, g.w2, f, d, E, 64, 64);
+      ok = (g.gather_rows != nullptr ? map2d(&p.g0, g.dy, d, T, 64, 1) : map2d(&p.a0, g.dy_perm, d, Tk, 64, 128)) &&
+           map3d(&p.b0, g.w2, f, d, E, 64, 64);
       if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 128) && map3d(&p.b1, g.ws2, fs, d, S, 64, 64);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<BWD2T>(p, num_sms, st);

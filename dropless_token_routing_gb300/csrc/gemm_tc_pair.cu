@@ -54,6 +54,7 @@ constexpr int SLAB = 64 * 128;          // one 64-element-wide, 64-row swizzled 
 
 struct PairParams {
   CUtensorMap a0, a1, b0, b1;  // operands (routed / shared), box {64, 64}
+  CUtensorMap g0;              // row gather of the routed token operand (dy or x, box {64, 1})
   CUtensorMap o0, o1;          // dW outputs (routed / shared), box {64, 32, 1}
   GroupedArgs g;
 };
@@ -109,11 +110,13 @@ __device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
 
 // ------------------------------------------------------------------ producer: TMA issue
 // This CTA's halves of K block kb: A = output rows [m0, m0+128), B = output columns
-// [n0, n0+128), both MN-major (the token copies run along K).
+// [n0, n0+128), both MN-major (the token copies run along K). `gather`: the token operand
+// (A = dY for dW2, B = x for dW13) is gathered by the whole producer warp instead
+// (issue_gather_half), so it is skipped here.
 template <int MODE>
 __device__ __forceinline__ void issue_half_loads(const PairParams& p, const TileCoord& tc, int kb,
                                                  uint32_t rank, uint32_t a_s, uint32_t b_s,
-                                                 uint32_t bar) {
+                                                 uint32_t bar, bool gather) {
   const GroupGeom& G = tc.G;
   const int T = (int)p.g.T;
   const int m0 = tc.mi * PM + HM * (int)rank;
@@ -124,10 +127,35 @@ __device__ __forceinline__ void issue_half_loads(const PairParams& p, const Tile
   const int kbr = G.shared ? ((MODE == DW2 ? G.s * T : 0) + k0) : row0 + k0;  // B rows
   const CUtensorMap* am = G.shared ? &p.a1 : &p.a0;
   const CUtensorMap* bm = G.shared ? &p.b1 : &p.b0;
+  if (!(gather && MODE == DW2)) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) tma2d(a_s + i * SLAB, am, bar, m0 + 64 * i, ka);
+    for (int i = 0; i < 2; ++i) tma2d(a_s + i * SLAB, am, bar, m0 + 64 * i, ka);
+  }
+  if (!(gather && MODE == DW13)) {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) tma2d(b_s + i * SLAB, bm, bar, n0 + 64 * i, kbr);
+    for (int i = 0; i < 2; ++i) tma2d(b_s + i * SLAB, bm, bar, n0 + 64 * i, kbr);
+  }
+}
+
+// Fused rearrangement of the token operand of a routed group: lane j fills rows
+// 4(j%16)..4(j%16)+3 of 64-column slab j/16 with the tokens of those permuted rows (rows
+// past the segment repeat its first row: the ragged K fix-up zeroes the matching A rows, so
+// they add nothing).
+template <int MODE>
+__device__ __forceinline__ void issue_gather_half(const PairParams& p, const TileCoord& tc, int kb,
+                                                  uint32_t rank, uint32_t a_s, uint32_t b_s,
+                                                  uint32_t bar, int lane) {
+  const GroupGeom& G = tc.G;
+  const int sl = lane >> 4, q = lane & 15;
+  int tok[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int k = kb * BK + 4 * q + i;
+    tok[i] = __ldg(p.g.gather_rows + G.row0 + (k < G.K ? k : 0));
+  }
+  const int c0 = MODE == DW13 ? tc.ni * BN + HN * (int)rank : tc.mi * PM + HM * (int)rank;
+  const uint32_t dst = (MODE == DW13 ? b_s : a_s) + sl * SLAB + q * 512;
+  tma_gather4(dst, &p.g0, bar, c0 + 64 * sl, tok[0], tok[1], tok[2], tok[3]);
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -243,6 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     for (int tile = pair; tile < total && ok; tile += npairs) {
       const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, PM, s_off);
       const int nkb = (tc.G.K + BK - 1) / BK;
+      const bool gather = a.gather_rows != nullptr && !tc.G.shared;
       for (int kb = 0; kb < nkb; ++kb) {
         const bool got = mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, &abort_flag, a.err,
                                            kWaitLimitNs);
@@ -251,7 +280,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const uint32_t bar = smem_u32(&land_bar[stage]);
         if (lane == 0) {
           mbar_arrive_expect_tx(bar, STAGE_BYTES);
-          issue_half_loads<MODE>(p, tc, kb, rank, a_s, b_s, bar);
+          issue_half_loads<MODE>(p, tc, kb, rank, a_s, b_s, bar, gather);
+        }
+        if (gather) {
+          __syncwarp();
+          issue_gather_half<MODE>(p, tc, kb, rank, a_s, b_s, bar, lane);
         }
         pending |= 1u << stage;
         pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
@@ -402,15 +435,17 @@ int launch_tc_pair_dw(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
   const uint64_t d = g.d, f = g.f, fs = g.f_s, E = g.E, S = g.S;
   const bool sh = g.S > 0;
   bool ok;
+  const bool gather = g.gather_rows != nullptr;
   if (mode == DW2) {
-    ok = map2d(&p.a0, g.dy_perm, d, Tk, 64, 64) && map2d(&p.b0, g.hw, f, Tk, 64, 64) &&
-         map3d(&p.o0, g.dw2, f, d, E, 64, 32);
+    ok = (gather ? map2d(&p.g0, g.dy, d, T, 64, 1) : map2d(&p.a0, g.dy_perm, d, Tk, 64, 64)) &&
+         map2d(&p.b0, g.hw, f, Tk, 64, 64) && map3d(&p.o0, g.dw2, f, d, E, 64, 32);
     if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 64) && map2d(&p.b1, g.hw_sh, fs, ST, 64, 64) &&
                  map3d(&p.o1, g.dws2, fs, d, S, 64, 32);
     if (!ok) return MOE_ERR_CUDA;
     return launch_pair<DW2>(p, num_sms, st);
   }
-  ok = map2d(&p.a0, g.dz, 2 * f, Tk, 64, 64) && map2d(&p.b0, g.x_perm, d, Tk, 64, 64) &&
+  ok = map2d(&p.a0, g.dz, 2 * f, Tk, 64, 64) &&
+       (gather ? map2d(&p.g0, g.x, d, T, 64, 1) : map2d(&p.b0, g.x_perm, d, Tk, 64, 64)) &&
        map3d(&p.o0, g.dw13, d, 2 * f, E, 64, 32);
   if (sh) ok = ok && map2d(&p.a1, g.dz_sh, 2 * fs, ST, 64, 64) && map2d(&p.b1, g.x, d, T, 64, 64) &&
                map3d(&p.o1, g.dws13, d, 2 * fs, S, 64, 32);

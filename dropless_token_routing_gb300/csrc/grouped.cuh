@@ -37,6 +37,10 @@ struct GroupedArgs {
   void *dw13, *dw2, *dws13, *dws2;
   const void* w_split;      // [E][3d] bf16: hi | mid | lo parts of W_r^T (ROUTER)
   float* logits_out;        // [T][E] fp32 (ROUTER)
+  // Fused rearrangement: when set (routed groups of FWD1, BWD2T, DW2, DW13, bf16), the
+  // permuted token rows are not read from x_perm / dy_perm but gathered from x / dy, row r
+  // of the permuted order being token gather_rows[r] (the permutation's row_src).
+  const int32_t* gather_rows;
   float* dgate_part;        // [n_tiles_f][Tk] per-N-tile partial sums of dgate (BWD2T)
   int64_t dgate_stride;     // = Tk
   int* err;

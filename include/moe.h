@@ -83,7 +83,16 @@ typedef struct moe_dims {
    * zero padding. The permuted buffers (x_perm, row_src, w_perm, z, h, y_perm, dy_perm,
    * dz, dx_perm) then have R = E*C rows instead of R = T*k, and offsets[e] = e*C. */
   int32_t capacity;
+  /* enum moe_rearrange: how the bf16 dropless layer feeds the permuted token rows to the
+   * expert GEMMs. MOE_REARRANGE_COPY (0, default): rearranged copies in memory (x_perm,
+   * dy_perm). MOE_REARRANGE_GATHER (1): the copies are fused into the GEMMs' operand loads
+   * (TMA row gathers from x and dy by row_src). On GB300 the gathers make the GEMMs about
+   * 2.5x slower than the copies cost, so the copy is the default. fp32 layers and the
+   * drop-and-pad variant always use copies. */
+  int32_t rearrange;
 } moe_dims;
+
+enum moe_rearrange { MOE_REARRANGE_COPY = 0, MOE_REARRANGE_GATHER = 1 };
 
 /* Human-readable text of a status code (static string). */
 const char* moe_status_string(int status);
@@ -241,7 +250,7 @@ typedef struct moe_layer_saved { /* caller-allocated; written by moe_layer_fwd, 
   int32_t* dest;     /* [T*k] */
   int32_t* row_src;  /* [T*k] */
   float* w_perm;     /* [T*k] */
-  void* x_perm;      /* [T*k, d], or NULL: selective recompute, the backward re-permutes x */
+  void* x_perm;      /* [T*k, d], or NULL: not kept (see below) */
   void* z;           /* [T*k, 2f] */
   void* h;           /* [T*k, f], or NULL: not kept (the backward recomputes h from z) */
   void* z_sh;        /* [S*T, 2f_s] or NULL when S == 0 */
@@ -250,8 +259,13 @@ typedef struct moe_layer_saved { /* caller-allocated; written by moe_layer_fwd, 
 /* Selective recompute (Pangu Ultra MoE tech-report article, memory section: permutation and
  * activation recomputed instead of saved; Huawei MoE training-operator article, Selective R/S):
  * with saved->x_perm, saved->h and saved->h_sh NULL the forward keeps them in the workspace
- * only, and the backward re-permutes x; the saved activations shrink by T*k*(d+f) + S*T*f_s
- * elements for one extra row move of x. Results are identical. */
+ * only; the saved activations shrink by T*k*(d+f) + S*T*f_s elements. Results are identical.
+ * With dims->rearrange = MOE_REARRANGE_GATHER (bf16, dropless) the rearrangement is fused
+ * into the expert GEMMs instead (Huawei MoE training-operator article, "VectorSort": cut
+ * repeated data movement): FWD1 and the dW13 product gather their x rows, the dX chain's
+ * first product and the dW2 product their dY rows, straight from x / dy by row_src. x_perm
+ * is then written only when the caller passes it, and dY is never rearranged in memory.
+ * Otherwise the backward re-permutes x when saved->x_perm is NULL. */
 
 typedef struct moe_layer_grads { /* caller-allocated outputs of moe_layer_bwd */
   void* dx;        /* [T, d]; includes the router term when w_r is given */

@@ -30,13 +30,14 @@ def _to(t, dev="cuda"):
     return None if t is None else t.to(dev)
 
 
-def run_gpu_layer(w, bwd=True, capacity=0):
+def run_gpu_layer(w, bwd=True, capacity=0, rearrange=0):
     from dropless_token_routing_gb300.api import LayerParams, MoELayer, get_device_error
     c = w.cfg
     params = LayerParams(w13=_to(w.w13), w2=_to(w.w2), w_r=_to(w.w_r), bias=_to(w.bias),
                          ws13=_to(w.ws13), ws2=_to(w.ws2))
     layer = MoELayer(params, c["T"], c["d"], c["E"], c["k"], c["f"], c["S"], c["f_s"],
-                     w.torch_dtype, logits_input=w.logits_in is not None, capacity=capacity)
+                     w.torch_dtype, logits_input=w.logits_in is not None, capacity=capacity,
+                     rearrange=rearrange)
     x = _to(w.x)
     layer.forward(x, _to(w.logits_in))
     grads = layer.backward(_to(w.dy)) if bwd else None
@@ -64,11 +65,11 @@ def oracle_layer(w, device_logits=None, bwd=True, capacity=0):
     return res
 
 
-def check_layer(w, bwd=True, report=None, capacity=0):
+def check_layer(w, bwd=True, report=None, capacity=0, rearrange=0):
     """Run both sides and assert every bar; returns a dict of the measured errors.
     capacity = C > 0 checks the drop-and-pad variant against the oracle's."""
     tol = TOL[w.cfg["dtype"]]
-    layer, grads, err = run_gpu_layer(w, bwd=bwd, capacity=capacity)
+    layer, grads, err = run_gpu_layer(w, bwd=bwd, capacity=capacity, rearrange=rearrange)
     assert err == 0, f"device error {err}"
     s = layer.saved
     errs = {}
