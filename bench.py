@@ -40,8 +40,8 @@ NCU_TRAFFIC = {
     # ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum (one pass)
     # on the default workload, one launch after warm-up; see profiles/gemm_dw13_pangu_bf16.md.
     # Applies only while the kernel's source file is unchanged since the capture.
-    "gemm_dw13": {"src": "gemm_tc_pair.cu", "bytes_per_launch": 2706356992 + 16168282624,
-                  "src_sha256": "9904b695397a28a2dfe999adf67361af41aefe3cb96e896ff417ca0f35a875eb"},
+    "gemm_dw13": {"src": "gemm_tc_pair.cu", "bytes_per_launch": 2886254080 + 16168128768,
+                  "src_sha256": "7a4471664184eeb96388d48bb4307e3fe0e8e07d0bf1474509511400b9c53f3d"},
 }
 
 

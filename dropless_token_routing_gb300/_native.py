@@ -86,6 +86,10 @@ _SIGS = {
     "moe_route_topk_bwd": (c_int, [P, P, P, c_int64, c_int32, c_int32, P, P]),
     "moe_route_balance": (c_int, [P, P, P, c_int64, c_int32, c_int32, ctypes.c_float, P, P, P, c_size_t, P]),
     "moe_route_balance_bwd": (c_int, [P, P, P, c_int64, c_int32, c_int32, ctypes.c_float, ctypes.c_float, P, P]),
+    "moe_route_balance_seq": (c_int, [P, P, P, c_int64, c_int32, c_int32, c_int64, ctypes.c_float, P, P, P, P,
+                                      c_size_t, P]),
+    "moe_route_balance_seq_bwd": (c_int, [P, P, P, c_int64, c_int32, c_int32, c_int64, c_int64,
+                                          ctypes.c_float, ctypes.c_float, P, P]),
     "moe_layer_fwd": (c_int, [ctypes.POINTER(LayerParams), P, P, ctypes.POINTER(MoeDims),
                               ctypes.POINTER(LayerSaved), P, P, c_size_t, P]),
     "moe_layer_bwd": (c_int, [ctypes.POINTER(LayerParams), ctypes.POINTER(LayerSaved), P, P,

@@ -142,6 +142,21 @@ def route_balance_bwd(logits, bias, counts, k, alpha, grad, dlogits, stream=None
             "moe_route_balance_bwd")
 
 
+def route_balance_seq(logits, bias, topk_idx, k, group_len, alpha, prob_mean, counts, aux_loss,
+                      ws: Workspace, stream=None):
+    T, E = logits.shape
+    N.check(N.lib().moe_route_balance_seq(_p(logits), _p(bias), _p(topk_idx), T, E, k, int(group_len),
+                                          float(alpha), _p(prob_mean), _p(counts), _p(aux_loss), ws.ptr,
+                                          ws.nbytes, _s(stream)), "moe_route_balance_seq")
+
+
+def route_balance_seq_bwd(logits, bias, counts, k, group_len, n_groups, alpha, grad, dlogits, stream=None):
+    T, E = logits.shape
+    N.check(N.lib().moe_route_balance_seq_bwd(_p(logits), _p(bias), _p(counts), T, E, k, int(group_len),
+                                              int(n_groups), float(alpha), float(grad), _p(dlogits),
+                                              _s(stream)), "moe_route_balance_seq_bwd")
+
+
 @dataclass
 class LayerParams:
     w13: torch.Tensor

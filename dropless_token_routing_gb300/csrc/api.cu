@@ -485,7 +485,51 @@ int moe_route_balance_bwd(const float* logits, const float* bias, const int32_t*
   MOE_TRY(req(counts));
   MOE_TRY(req(dlogits));
   const double scale = (double)grad * alpha * E / ((double)T * (double)T * (double)k);
-  MOE_LAUNCH(launch_balance_bwd(logits, bias, counts, T, E, (float)scale, dlogits, (cudaStream_t)stream));
+  MOE_LAUNCH(launch_balance_bwd(logits, bias, counts, T, E, T, (float)scale, dlogits, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+int moe_route_balance_seq(const float* logits, const float* bias, const int32_t* topk_idx, int64_t T,
+                          int32_t E, int32_t k, int64_t group_len, float alpha, float* prob_mean,
+                          int32_t* counts, float* aux_loss, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
+  if (E < 1 || E > kMaxE || T < 1 || T > (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
+  if (k < 1 || k > E || k > kMaxK) return MOE_ERR_BAD_TOPK;
+  if (group_len < 1 || T % group_len != 0 || T / group_len > 65535) return MOE_ERR_BAD_DIMS;
+  if (ws == nullptr) return MOE_ERR_NULL_POINTER;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_MISALIGNED;
+  const int64_t G = T / group_len;
+  const size_t part_bytes = sizeof(float) * (size_t)G * balance_group_chunks(group_len) * E;
+  if (ws_bytes < 256 + part_bytes + sizeof(float) * (size_t)G) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  MOE_TRY(req(logits));
+  MOE_TRY(opt(bias));
+  MOE_TRY(req(topk_idx));
+  MOE_TRY(opt(prob_mean));
+  MOE_TRY(req(counts));
+  MOE_TRY(req(aux_loss));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* part = reinterpret_cast<float*>(w + 256);
+  float* gterm = reinterpret_cast<float*>(w + 256 + part_bytes);
+  MOE_LAUNCH(launch_balance_groups(logits, bias, topk_idx, T, E, k, group_len, alpha, part, gterm, prob_mean,
+                                   counts, aux_loss, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+int moe_route_balance_seq_bwd(const float* logits, const float* bias, const int32_t* counts, int64_t T,
+                              int32_t E, int32_t k, int64_t group_len, int64_t n_groups, float alpha,
+                              float grad, float* dlogits, moe_stream_t stream) {
+  if (E < 1 || E > kMaxE || T < 0 || T > (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
+  if (k < 1 || k > E || k > kMaxK) return MOE_ERR_BAD_TOPK;
+  if (group_len < 1 || n_groups < 1) return MOE_ERR_BAD_DIMS;
+  if (T == 0) return MOE_OK;
+  MOE_TRY(req(logits));
+  MOE_TRY(opt(bias));
+  MOE_TRY(req(counts));
+  MOE_TRY(req(dlogits));
+  const double scale =
+      (double)grad * alpha * E / ((double)n_groups * (double)group_len * (double)group_len * (double)k);
+  MOE_LAUNCH(launch_balance_bwd(logits, bias, counts, T, E, group_len, (float)scale, dlogits,
+                                (cudaStream_t)stream));
   return MOE_OK;
 }
 
@@ -672,17 +716,22 @@ int moe_layer_bwd(const moe_layer_params* params, const moe_layer_saved* saved, 
   MOE_LAUNCH(launch_route_bwd(saved->topk_idx, saved->topk_w, nullptr, dgate_part, dgate_tiles(dims),
                               a.Tk, saved->dest, cap ? dest_full : saved->dest, dims->T, dims->E,
                               dims->k, dgate, grads->dlogits, dl_tok, dl_perm, st));
-  // 4. expert dX chain, second half: dx_perm = dz W13
-  a.dz = dz; a.dz_sh = dz_sh; a.dx_perm = dx_perm; a.dx_sh = dx_sh;
-  MOE_TRY(run_grouped(BWD1T, a, dims, st));
-  // 5. un-rearrange dX (+ shared dX, + router term dl W_r^T)
+  // 4. expert dX chain, second half: dx_perm = dz W13. On the bf16 dropless path the router
+  //    term dl W_r^T of each copy is added to its row here (every copy has a row); fp32 and
+  //    drop-and-pad (dropped copies have no row) add it in the un-rearrangement instead.
   const float* w_rT = nullptr;
   if (router) {
     MOE_LAUNCH(launch_transpose_f32(params->w_r, dims->d, dims->E, reinterpret_cast<float*>(w + L.w_rT), st));
     w_rT = reinterpret_cast<const float*>(w + L.w_rT);
   }
-  MOE_LAUNCH(launch_combine(dx_perm, saved->dest, nullptr, dx_sh, saved->topk_idx, dl_tok, w_rT, *dims,
-                            grads->dx, st));
+  const bool fold_router = router && dims->dtype == MOE_BF16 && !cap;
+  a.dz = dz; a.dz_sh = dz_sh; a.dx_perm = dx_perm; a.dx_sh = dx_sh;
+  a.dl_perm = dl_perm;
+  a.w_rT = fold_router ? w_rT : nullptr;
+  MOE_TRY(run_grouped(BWD1T, a, dims, st));
+  // 5. un-rearrange dX (+ shared dX, + the router term when not folded above)
+  MOE_LAUNCH(launch_combine(dx_perm, saved->dest, nullptr, dx_sh, saved->topk_idx, dl_tok,
+                            fold_router ? nullptr : w_rT, *dims, grads->dx, st));
   // 6. expert dW products (separate kernels from the dX chain)
   const void* x_perm = saved->x_perm;
   if (x_perm == nullptr && !gather) {  // selective recompute of the rearranged input

@@ -320,11 +320,27 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileCoord
     else
       out = G.shared ? (__nv_bfloat16*)a.dx_sh + (int64_t)m * a.d
                      : (__nv_bfloat16*)a.dx_perm + (G.row0 + m) * (int64_t)a.d;
+    // router term of the x-gradient folded into the routed dx rows: row q of expert e gets
+    // dl_q * W_r^T[e] (the segment shares one router row, read from L1)
+    const bool router = MODE == BWD1T && a.w_rT != nullptr && !G.shared;
+    const float dl = router && row_ok ? __ldg(a.dl_perm + G.row0 + m) : 0.f;
+    const float* wr = router ? a.w_rT + (int64_t)G.e * a.d + n0 : nullptr;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 64) {
       if (n0 + c >= G.N) break;
       float v[64];
       tmem_ld64(acc + c, v);
+      if (router) {
+        const float4* w4 = reinterpret_cast<const float4*>(wr + c);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 t = __ldg(w4 + i);
+          v[4 * i] = fmaf(dl, t.x, v[4 * i]);
+          v[4 * i + 1] = fmaf(dl, t.y, v[4 * i + 1]);
+          v[4 * i + 2] = fmaf(dl, t.z, v[4 * i + 2]);
+          v[4 * i + 3] = fmaf(dl, t.w, v[4 * i + 3]);
+        }
+      }
       pack64(v, pk);
       warp_store_chunk(stage, lane, pk, row_or_null(row_ok, out + n0 + c));
     }

@@ -41,6 +41,10 @@ struct GroupedArgs {
   // permuted token rows are not read from x_perm / dy_perm but gathered from x / dy, row r
   // of the permuted order being token gather_rows[r] (the permutation's row_src).
   const int32_t* gather_rows;
+  // BWD1T: when w_rT is set, routed row q also gets dl_perm[q] * w_rT[e] (the router term
+  // of the x-gradient, so that the un-rearrangement need not add it)
+  const float* dl_perm;     // [Tk] score gradient of each permuted row
+  const float* w_rT;        // [E][d] fp32 router weight, transposed
   float* dgate_part;        // [n_tiles_f][Tk] per-N-tile partial sums of dgate (BWD2T)
   int64_t dgate_stride;     // = Tk
   int* err;

@@ -95,7 +95,13 @@ cudaError_t launch_balance(const float* logits, const float* bias, const int32_t
                            int E, int k, float alpha, float* part, float* prob_mean, float* aux_loss,
                            cudaStream_t st);
 cudaError_t launch_balance_bwd(const float* logits, const float* bias, const int32_t* counts,
-                               int64_t T, int E, float scale, float* dlogits, cudaStream_t st);
+                               int64_t T, int E, int64_t group_len, float scale, float* dlogits,
+                               cudaStream_t st);
+int balance_group_chunks(int64_t group_len);
+cudaError_t launch_balance_groups(const float* logits, const float* bias, const int32_t* idx, int64_t T,
+                                  int E, int k, int64_t group_len, float alpha, float* part,
+                                  float* gterm, float* prob_mean, int32_t* counts, float* aux_loss,
+                                  cudaStream_t st);
 cudaError_t launch_transpose_f32(const float* in, int rows, int cols, float* out, cudaStream_t st);
 cudaError_t launch_dwr(const void* x, const int32_t* row_src, const float* dl_perm,
                        const int32_t* offsets, const moe_dims& dm, float* part, float* dw_r,

@@ -312,16 +312,125 @@ __global__ void __launch_bounds__(1024) balance_final_kernel(const float* __rest
   }
 }
 
-// dlogits[t, e] += scale * p_te * (counts_e - sum_e' counts_e' p_te'),
-// scale = grad * alpha * E / (T * T * k). One warp per token.
+// Sequence-level statistics: groups of group_len consecutive tokens. Block (c, g) sums the
+// softmax probabilities of a fixed slice of group g's tokens (one warp per token, fixed order)
+// into part[g][c][E] and counts the group's top-k choices (integer atomics: exact, so the
+// result does not depend on their order).
+template <int V>
+__global__ void __launch_bounds__(256) balance_group_partial_kernel(
+    const float* __restrict__ logits, const float* __restrict__ bias, const int32_t* __restrict__ idx,
+    int E, int k, int64_t group_len, float* __restrict__ part, int32_t* __restrict__ counts) {
+  __shared__ float wsum[8][kMaxE];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int64_t g = blockIdx.y, t0 = g * group_len;
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  for (int64_t u = (int64_t)blockIdx.x * nw + warp; u < group_len; u += (int64_t)gridDim.x * nw) {
+    const int64_t t = t0 + u;
+    float v[V];
+    float m = -FLT_MAX;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = -FLT_MAX;
+      if (e < E) {
+        float s = __ldg(logits + t * E + e);
+        if (bias != nullptr) s = s + __ldg(bias + e);
+        v[i] = s;
+        m = fmaxf(m, s);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      v[i] = (lane + 32 * i < E) ? expf(v[i] - m) : 0.f;
+      z += v[i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const float inv = 1.f / z;
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = fmaf(v[i], inv, acc[i]);
+    if (lane < k) {
+      const int e = __ldg(idx + t * k + lane);
+      if (e >= 0 && e < E) atomicAdd(counts + g * E + e, 1);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < V; ++i)
+    if (lane + 32 * i < E) wsum[warp][lane + 32 * i] = acc[i];
+  __syncthreads();
+  float* out = part + ((int64_t)g * gridDim.x + blockIdx.x) * E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float s = 0.f;
+    for (int w = 0; w < nw; ++w) s += wsum[w][e];
+    out[e] = s;
+  }
+}
+
+// One block per group: P_ge = (sum of the group's block rows) / group_len and the group's
+// term sum_e counts_ge * P_ge.
+__global__ void __launch_bounds__(1024) balance_group_final_kernel(
+    const float* __restrict__ part, int nchunks, const int32_t* __restrict__ counts, int E,
+    int64_t group_len, float* __restrict__ prob_mean, float* __restrict__ gterm) {
+  __shared__ float red[32];
+  const int64_t g = blockIdx.x;
+  const int e = threadIdx.x;
+  float term = 0.f;
+  if (e < E) {
+    float s = 0.f;
+    for (int c = 0; c < nchunks; ++c) s += part[(g * nchunks + c) * E + e];
+    const float P = s / (float)group_len;
+    if (prob_mean != nullptr) prob_mean[g * E + e] = P;
+    term = (float)counts[g * E + e] * P;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+  if (lane == 0) red[warp] = term;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
+    gterm[g] = s;
+  }
+}
+
+// L_aux = alpha * E / (G * group_len * k) * sum_g term_g, summed in group order by one thread
+// per 1024-group stripe and then a fixed shuffle tree.
+__global__ void __launch_bounds__(1024) balance_group_loss_kernel(const float* __restrict__ gterm,
+                                                                  int64_t G, float scale,
+                                                                  float* __restrict__ aux_loss) {
+  __shared__ float red[32];
+  float s = 0.f;
+  for (int64_t g = threadIdx.x; g < G; g += blockDim.x) s += gterm[g];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) red[warp] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+    aux_loss[0] = scale * t;
+  }
+}
+
+// dlogits[t, e] += scale * p_te * (c_e - sum_e' c_e' p_te'), c = the counts of token t's group
+// (group t / group_len), scale = grad * alpha * E / (n_groups * group_len^2 * k). One warp per
+// token.
 template <int V>
 __global__ void __launch_bounds__(256) balance_bwd_kernel(const float* __restrict__ logits,
                                                           const float* __restrict__ bias,
-                                                          const int32_t* __restrict__ counts,
-                                                          int64_t T, int E, float scale,
-                                                          float* __restrict__ dlogits) {
+                                                          const int32_t* __restrict__ counts_all,
+                                                          int64_t T, int E, int64_t group_len,
+                                                          float scale, float* __restrict__ dlogits) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < T; t += (int64_t)gridDim.x * nw) {
+    const int32_t* counts = counts_all + (t / group_len) * E;   // the token's group
     float v[V], c[V];
     float m = -FLT_MAX;
 #pragma unroll
@@ -539,12 +648,38 @@ cudaError_t launch_balance(const float* logits, const float* bias, const int32_t
 }
 
 cudaError_t launch_balance_bwd(const float* logits, const float* bias, const int32_t* counts,
-                               int64_t T, int E, float scale, float* dlogits, cudaStream_t st) {
+                               int64_t T, int E, int64_t group_len, float scale, float* dlogits,
+                               cudaStream_t st) {
   int64_t blocks = (T + 7) / 8;
   if (blocks > 65535) blocks = 65535;
   TraceScope ts(TP_MISC, st);
   MOE_V_DISPATCH(E, (balance_bwd_kernel<VV><<<(unsigned)blocks, 256, 0, st>>>(logits, bias, counts, T, E,
-                                                                               scale, dlogits)));
+                                                                               group_len, scale, dlogits)));
+  return cudaGetLastError();
+}
+
+int balance_group_chunks(int64_t group_len) {
+  int64_t c = (group_len + 63) / 64;
+  return (int)(c < 32 ? (c < 1 ? 1 : c) : 32);
+}
+
+cudaError_t launch_balance_groups(const float* logits, const float* bias, const int32_t* idx, int64_t T,
+                                  int E, int k, int64_t group_len, float alpha, float* part,
+                                  float* gterm, float* prob_mean, int32_t* counts, float* aux_loss,
+                                  cudaStream_t st) {
+  const int64_t G = T / group_len;
+  const int nc = balance_group_chunks(group_len);
+  TraceScope ts(TP_MISC, st);
+  if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)G * E, st) != cudaSuccess) return cudaErrorUnknown;
+  MOE_V_DISPATCH(E, (balance_group_partial_kernel<VV><<<dim3(nc, (unsigned)G), 256, 0, st>>>(
+                        logits, bias, idx, E, k, group_len, part, counts)));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  balance_group_final_kernel<<<(unsigned)G, 1024, 0, st>>>(part, nc, counts, E, group_len, prob_mean, gterm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const double scale = (double)alpha * E / ((double)G * (double)group_len * (double)k);
+  balance_group_loss_kernel<<<1, 1024, 0, st>>>(gterm, G, (float)scale, aux_loss);
   return cudaGetLastError();
 }
 

@@ -231,6 +231,30 @@ int moe_route_balance_bwd(const float* logits, const float* bias, const int32_t*
                           int32_t E, int32_t k, float alpha, float grad, float* dlogits,
                           moe_stream_t stream);
 
+/* Sequence-level form of the balance statistics (same pages): the T tokens fall into
+ * G = T / group_len groups of consecutive tokens (one sequence each; T % group_len == 0,
+ * G <= 65535), each with its own term, and the loss is their mean:
+ *   P_ge = (1/group_len) sum_{t in g} softmax(s_t)_e,   f_ge = counts_ge / (group_len k)
+ *   L_aux = alpha * E / G * sum_g sum_e f_ge P_ge
+ * group_len = T is the micro-batch form above. topk_idx [T][k] -> counts [G][E] int32 (each
+ * group's top-k choices), prob_mean [G][E] fp32 (or NULL), aux_loss [1] fp32. For the
+ * global-batch (data-parallel group) and expert-parallel-group forms the caller sums counts
+ * (and averages prob_mean) over the ranks of the group and passes the summed counts to the
+ * backward with group_len = the group's token count and n_groups = 1.
+ * ws: >= 256 + 4*G*(E*min(32, ceil(group_len/64)) + 1) bytes, 256-byte aligned. */
+int moe_route_balance_seq(const float* logits, const float* bias, const int32_t* topk_idx, int64_t T,
+                          int32_t E, int32_t k, int64_t group_len, float alpha, float* prob_mean,
+                          int32_t* counts, float* aux_loss, void* ws, size_t ws_bytes,
+                          moe_stream_t stream);
+
+/* Gradient of grad * L_aux (sequence-level form) w.r.t. the scores, ADDED into dlogits:
+ *   dlogits[t,e] += grad * alpha * E / (n_groups * group_len^2 * k) * p_te *
+ *                   (c_ge - sum_e' c_ge' p_te'),   g = t / group_len,
+ * counts c [ceil(T/group_len)][E] (constants of the gradient). */
+int moe_route_balance_seq_bwd(const float* logits, const float* bias, const int32_t* counts, int64_t T,
+                              int32_t E, int32_t k, int64_t group_len, int64_t n_groups, float alpha,
+                              float grad, float* dlogits, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- whole layer */
 typedef struct moe_layer_params {
   const float* w_r;  /* [d][E] fp32, or NULL when the caller passes logits_in */

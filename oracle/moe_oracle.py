@@ -52,7 +52,8 @@ __all__ = [
     "silu", "silu_grad", "router_logits", "selection_scores", "route_topk",
     "expert_counts", "expert_offsets", "permutation", "capacity_permutation", "swiglu_rows",
     "layer_forward", "layer_backward", "router_backward", "as_f64",
-    "balance_loss", "balance_loss_grad", "coefficient_of_variation",
+    "balance_loss", "balance_loss_grad", "balance_loss_groups", "balance_loss_groups_grad",
+    "coefficient_of_variation",
 ]
 
 
@@ -368,6 +369,39 @@ def balance_loss_grad(scores, counts, k, alpha):
     f = np.asarray(counts, np.float64) / (T * k)
     inner = (p * f[None, :]).sum(axis=1, keepdims=True)
     return alpha * E / T * p * (f[None, :] - inner)
+
+
+def balance_loss_groups(scores, idx, k, alpha, group_len, n_groups=None, counts=None):
+    """Sequence-level form: the tokens fall into groups of ``group_len`` consecutive tokens
+    (one sequence each) and each group has its own balance term; the loss is their mean,
+    ``L = alpha * E / n_groups * sum_g sum_e f_ge * P_ge`` with ``f_ge = counts_ge /
+    (group_len * k)`` and ``P_ge`` the group's mean softmax probability. ``group_len = T``
+    is the micro-batch form of :func:`balance_loss`. ``counts [G, E]`` may be given (e.g.
+    summed over the ranks of a data-parallel group); by default they are the groups' own
+    top-k counts. Returns (P [G, E], counts [G, E], L)."""
+    p = _softmax_rows(scores)
+    T, E = p.shape
+    assert T % group_len == 0
+    G = T // group_len
+    n_groups = G if n_groups is None else n_groups
+    P = p.reshape(G, group_len, E).mean(axis=1)
+    if counts is None:
+        counts = np.stack([expert_counts(np.asarray(idx)[g * group_len:(g + 1) * group_len], E)
+                           for g in range(G)])
+    f = np.asarray(counts, np.float64) / (group_len * k)
+    return P, counts, alpha * E / n_groups * float(np.sum(f * P))
+
+
+def balance_loss_groups_grad(scores, counts, k, alpha, group_len, n_groups=None):
+    """d L / d scores [T, E] of :func:`balance_loss_groups`, counts held constant."""
+    p = _softmax_rows(scores)
+    T, E = p.shape
+    G = -(-T // group_len)
+    n_groups = G if n_groups is None else n_groups
+    f = np.asarray(counts, np.float64).reshape(-1, E) / (group_len * k)
+    fg = f[np.arange(T) // group_len]                     # each token's group
+    inner = (p * fg).sum(axis=1, keepdims=True)
+    return alpha * E / (n_groups * group_len) * p * (fg - inner)
 
 
 def coefficient_of_variation(counts):

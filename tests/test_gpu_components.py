@@ -232,3 +232,37 @@ def test_balance_statistics_and_gradient_match_oracle():
     expect = base + d0.cpu()
     tol = 2 * torch.finfo(torch.float32).eps * (base.abs() + d0.cpu().abs()) + 1e-38
     assert torch.all((d.cpu() - expect).abs() <= tol)
+
+
+@pytest.mark.parametrize("T,E,k,L", [(1024, 64, 6, 256), (1000, 24, 3, 1000), (4096, 256, 8, 512)])
+def test_balance_sequence_level_matches_oracle(T, E, k, L):
+    """moe_route_balance_seq / _bwd (groups of L consecutive tokens) against the oracle."""
+    A = _api()
+    g = torch.Generator().manual_seed(T + L)
+    Lg = torch.randn(T, E, generator=g) * 2
+    bias = torch.randn(E, generator=g) * 0.5
+    s32 = O.selection_scores(Lg.numpy(), bias.numpy())
+    idx, _ = O.route_topk(s32, k)
+    P_ref, c_ref, l_ref = O.balance_loss_groups(s32, idx, k, 0.01, L)
+    G = T // L
+    dims = A.make_dims(T, 64, E, k, 64, dtype=torch.float32)
+    ws = A.Workspace(dims)
+    lg, bg = Lg.cuda(), bias.cuda()
+    ig = torch.as_tensor(idx, dtype=torch.int32).cuda()
+    P = torch.empty(G, E, device="cuda")
+    counts = torch.full((G, E), 7, dtype=torch.int32, device="cuda")
+    aux = torch.empty(1, device="cuda")
+    outs = []
+    for _ in range(2):   # deterministic: the same bits twice
+        A.route_balance_seq(lg, bg, ig, k, L, 0.01, P, counts, aux, ws)
+        torch.cuda.synchronize()
+        outs.append((P.clone(), counts.clone(), aux.clone()))
+    assert all(torch.equal(a, b) for a, b in zip(outs[0], outs[1]))
+    assert np.array_equal(counts.cpu().numpy(), c_ref)
+    assert np.linalg.norm(P.cpu().double().numpy() - P_ref) / np.linalg.norm(P_ref) <= 1e-5
+    assert abs(aux.item() - l_ref) / abs(l_ref) <= 1e-5
+    d0 = torch.zeros(T, E, device="cuda")
+    A.route_balance_seq_bwd(lg, bg, counts, k, L, G, 0.01, 1.3, d0)
+    torch.cuda.synchronize()
+    ref = 1.3 * O.balance_loss_groups_grad(s32, c_ref, k, 0.01, L)
+    assert np.linalg.norm(d0.cpu().double().numpy() - ref) / np.linalg.norm(ref) <= 1e-5

@@ -128,8 +128,10 @@ def test_capacity_layer_matches_oracle(case, cf):
 
 def test_capacity_at_max_count_reproduces_dropless_rows():
     """With C = the largest expert count nothing is dropped: every row's forward result is
-    the dropless one bit for bit (a row's products do not depend on where it sits), and dx
-    too; the dW products reduce over zero padding rows as well and agree to rounding."""
+    the dropless one bit for bit (a row's products do not depend on where it sits). dx agrees
+    to rounding: the dropless bf16 path adds the router term to each dx row in the dX GEMM
+    epilogue, the drop-and-pad path in the un-rearrangement. The dW products reduce over zero
+    padding rows as well and agree to rounding."""
     from layer_check import run_gpu_layer
     w = make_workload(shrink("pangu_bf16", T=640, d=512, E=16, k=4, f=256, f_s=256))
     ref, gr, e0 = run_gpu_layer(w)
@@ -138,10 +140,9 @@ def test_capacity_at_max_count_reproduces_dropless_rows():
     assert e0 == 0 and e1 == 0
     assert (cap.saved["dest"] >= 0).all()
     assert torch.equal(ref.y, cap.y)
-    assert torch.equal(gr["dx"], gc["dx"])
-    for n in ("dw13", "dw2", "dws13", "dws2"):
+    for n, tol in (("dx", 5e-3), ("dw13", 2e-3), ("dw2", 2e-3), ("dws13", 2e-3), ("dws2", 2e-3)):
         a, b = gr[n].float(), gc[n].float()
-        assert (torch.linalg.norm(a - b) / torch.linalg.norm(a)).item() <= 2e-3, n
+        assert (torch.linalg.norm(a - b) / torch.linalg.norm(a)).item() <= tol, n
     assert torch.allclose(gr["dw_r"], gc["dw_r"], rtol=1e-5, atol=1e-6)
 
 

@@ -356,6 +356,43 @@ def test_balance_loss_gradient_central_differences():
     np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-14)   # softmax Jacobian rows sum to 0
 
 
+def test_balance_groups_reduce_and_average():
+    """One group of all T tokens is the micro-batch form; G groups average their own
+    micro-batch terms (each evaluated on its slice alone)."""
+    rng = np.random.default_rng(13)
+    T, E, k, L = 48, 7, 2, 12
+    s = rng.standard_normal((T, E)) * 1.5
+    idx, _ = O.route_topk(s, k)
+    P1, c1, l1 = O.balance_loss_groups(s, idx, k, 0.2, T)
+    P0, l0 = O.balance_loss(s, O.expert_counts(idx, E), k, 0.2)
+    np.testing.assert_allclose(P1[0], P0, rtol=1e-14)
+    np.testing.assert_allclose(l1, l0, rtol=1e-14)
+    P, c, lg = O.balance_loss_groups(s, idx, k, 0.2, L)
+    per = [O.balance_loss(s[g * L:(g + 1) * L], O.expert_counts(idx[g * L:(g + 1) * L], E), k, 0.2)[1]
+           for g in range(T // L)]
+    np.testing.assert_allclose(lg, np.mean(per), rtol=1e-14)
+    assert c.sum() == T * k and np.all(c.sum(axis=1) == L * k)
+
+
+def test_balance_groups_gradient_central_differences():
+    rng = np.random.default_rng(14)
+    T, E, k, L = 12, 5, 2, 4
+    s = rng.standard_normal((T, E))
+    idx, _ = O.route_topk(s, k)
+    _, counts, _ = O.balance_loss_groups(s, idx, k, 0.3, L)
+    g = O.balance_loss_groups_grad(s, counts, k, 0.3, L)
+    num = np.zeros_like(s)
+    h = 1e-6
+    for t in range(T):
+        for e in range(E):
+            sp, sm = s.copy(), s.copy()
+            sp[t, e] += h
+            sm[t, e] -= h
+            num[t, e] = (O.balance_loss_groups(sp, idx, k, 0.3, L, counts=counts)[2] -
+                         O.balance_loss_groups(sm, idx, k, 0.3, L, counts=counts)[2]) / (2 * h)
+    assert np.linalg.norm(num - g) / np.linalg.norm(g) < 1e-7
+
+
 # ---------------------------------------------------------------- drop-and-pad pins
 def _kept_brute(idx, C):
     """Copy (t, j) is kept iff fewer than C copies of its expert come before it in
