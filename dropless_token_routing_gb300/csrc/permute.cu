@@ -123,11 +123,13 @@ template <typename T, int U>
 __device__ __forceinline__ void copy_row_to_dests(const T* __restrict__ src, T* __restrict__ dst,
                                                   int d, int k, int dq, int lane) {
   const int nvec = d / 8;
-  for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+  // the loop is uniform across the warp (every lane takes part in every shuffle, also when
+  // the row has fewer than 32 * U vectors left); loads and stores are predicated
+  for (int base = 0; base < nvec; base += 32 * U) {
     Vec8<T> val[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int v = v0 + 32 * u;
+      const int v = base + lane + 32 * u;
       if (v < nvec) val[u].load(src + (int64_t)v * 8);
     }
     for (int j = 0; j < k; ++j) {
@@ -136,7 +138,7 @@ __device__ __forceinline__ void copy_row_to_dests(const T* __restrict__ src, T* 
       T* drow = dst + (int64_t)dj * d;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int v = v0 + 32 * u;
+        const int v = base + lane + 32 * u;
         if (v < nvec) val[u].store(drow + (int64_t)v * 8);
       }
     }
@@ -232,12 +234,15 @@ __global__ void __launch_bounds__(256) combine_kernel(
         gq = dl_tok[q];
       }
     }
-    for (int v = lane; v < nvec; v += 32) {
+    // uniform across the warp: every lane takes part in every shuffle; accesses predicated
+    for (int vb = 0; vb < nvec; vb += 32) {
+      const int v = vb + lane;
+      const bool on = v < nvec;
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int j = 0; j < k; ++j) {
         const int dj = __shfl_sync(0xffffffffu, dq, j);
         const float wj = __shfl_sync(0xffffffffu, wq, j);
-        if (dj < 0) continue;
+        if (dj < 0 || !on) continue;
         Vec8<T> val;
         val.load(y_perm + (int64_t)dj * d + (int64_t)v * 8);
         float f[8];
@@ -245,7 +250,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
       }
-      if (y_sh != nullptr) {
+      if (y_sh != nullptr && on) {
         Vec8<T> val;
         val.load(y_sh + t * d + (int64_t)v * 8);
         float f[8];
@@ -257,6 +262,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
         for (int j = 0; j < k; ++j) {
           const int ej = __shfl_sync(0xffffffffu, eq, j);
           const float gj = __shfl_sync(0xffffffffu, gq, j);
+          if (!on) continue;
           const float4* wr = reinterpret_cast<const float4*>(w_rT + (int64_t)ej * d + (int64_t)v * 8);
           const float4 p0 = __ldg(wr), p1 = __ldg(wr + 1);
           acc[0] = fmaf(gj, p0.x, acc[0]); acc[1] = fmaf(gj, p0.y, acc[1]);
@@ -265,9 +271,11 @@ __global__ void __launch_bounds__(256) combine_kernel(
           acc[6] = fmaf(gj, p1.z, acc[6]); acc[7] = fmaf(gj, p1.w, acc[7]);
         }
       }
-      Vec8<T> out;
-      out.from_float(acc);
-      out.store(y + t * d + (int64_t)v * 8);
+      if (on) {
+        Vec8<T> out;
+        out.from_float(acc);
+        out.store(y + t * d + (int64_t)v * 8);
+      }
     }
   }
 }

@@ -139,6 +139,37 @@ def test_capacity_permute_matches_oracle(T, E, k, C):
     assert np.array_equal(w_perm.cpu().numpy(), wp)
 
 
+@pytest.mark.parametrize("d,k,E", [(64, 16, 40), (1088, 12, 32), (448, 30, 64)])
+def test_row_moves_when_a_row_ends_mid_warp(d, k, E):
+    """Rows whose 16-byte vectors do not fill whole warp passes (d/8 = 8, 136, 56) with more
+    copies per token than active lanes in the last pass: the scatter, the gather-only move and
+    both combines must still place every copy."""
+    A = _api()
+    T = 300
+    g = torch.Generator().manual_seed(d + k)
+    idx, _ = O.route_topk(torch.randn(T, E, generator=g).numpy(), k)
+    gate = torch.rand(T, k, generator=g)
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    dims = A.make_dims(T, d, E, k, 64, dtype=torch.bfloat16)
+    ws = A.Workspace(dims)
+    x_perm = torch.zeros(T * k, d, dtype=torch.bfloat16, device="cuda")
+    dest = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    row_src = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    A.permute(x.cuda(), torch.as_tensor(idx, dtype=torch.int32).cuda(), gate.cuda(), dims, x_perm, dest,
+              row_src, offsets, None, ws)
+    assert A.get_device_error(ws) == 0
+    rdest, rsrc = O.permutation(idx, E)
+    assert torch.equal(x_perm.cpu(), x[torch.as_tensor(rsrc)])
+    again = torch.zeros_like(x_perm)
+    A.permute_rows(x.cuda(), dest, dims, again)
+    assert torch.equal(again, x_perm)
+    y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    A.unpermute_combine(x_perm, dest, gate.cuda(), x.cuda(), dims, y)
+    ref = O.as_f64(x) * (gate.double().sum(1, keepdim=True).numpy() + 1.0)
+    assert np.linalg.norm(O.as_f64(y) - ref) / np.linalg.norm(ref) <= 5e-3
+
+
 def test_permute_rejects_bad_expert_ids_without_writing_out_of_bounds():
     T, E, k = 200, 8, 2
     g = torch.Generator().manual_seed(3)

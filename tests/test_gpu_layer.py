@@ -168,3 +168,17 @@ def test_fused_gather_matches_copies_bitwise():
     assert torch.equal(a.y, b.y) and torch.equal(a.saved["z"], b.saved["z"])
     for n in ("dx", "dw13", "dw2", "dws13", "dws2", "dw_r"):
         assert torch.equal(ga[n], gb[n]), n
+
+
+# ---------------------------------------------------------------- limits
+@pytest.mark.parametrize("case", ["bf16", "fp32"])
+def test_layer_at_the_expert_and_topk_limits(case):
+    """E = 1024 experts and k = 32 per token (the library's maxima): the chunk masks, the
+    1024-wide scans, the 32-column top-k registers and the 1032-group tile schedule at full
+    width, with most experts holding 0-3 rows; T = 333 leaves a ragged last chunk."""
+    from layer_check import check_layer
+    if case == "bf16":
+        cfg = shrink("pangu_bf16", T=333, d=128, E=1024, k=32, f=64, f_s=64)
+    else:
+        cfg = shrink("tiny_fp32", T=333, d=64, E=1024, k=32, f=64)
+    check_layer(make_workload(cfg), bwd=True)
