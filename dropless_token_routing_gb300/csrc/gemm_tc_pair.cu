@@ -12,18 +12,18 @@
 // with a single CTA per 128 x 256 tile: a third less L2->SM traffic per FLOP, and room for
 // six pipeline stages instead of four.
 //
-// Roles in each CTA of the pair (7 warps):
-//   warp 0      TMA producer: this CTA's A and B halves into the 6-stage ring; the bytes
-//               complete on this CTA's land_bar
+// Roles in each CTA of the pair (3 + EW warps, EW = 4 or 8 epilogue warps):
+//   warp 0      TMA producer: this CTA's A and B halves into the 6- (or 5-) stage ring; the
+//               bytes complete on this CTA's land_bar
 //   warp 1      TMEM owner (the pair allocates together); in the even CTA the lane-0 thread
 //               issues the MMAs of the pair
-//   warps 2..5  epilogue: TMEM -> bf16 -> 128-byte swizzled staging -> TMA tensor store
-//   warp 6      relay: waits until this CTA's K block has landed, zeroes the A rows past a
+//   warps 2..   epilogue: TMEM -> bf16 -> 128-byte swizzled staging -> TMA tensor store
+//   last warp   relay: waits until this CTA's K block has landed, zeroes the A rows past a
 //               ragged expert segment, then arrives on the even CTA's full_bar, which
 //               therefore completes once both halves of the K block are in place
 // The issuer's commits arrive on the stage and accumulator barriers of both CTAs
 // (multicast); each epilogue warp of either CTA frees an accumulator buffer by arriving on
-// the even CTA's tempty_bar (8 arrivals).
+// the even CTA's tempty_bar (2 * EW arrivals).
 // Every mbarrier wait is bounded (1 s). On expiry the CTA records MOE_ERR_DEVICE_TIMEOUT and
 // winds down: its producer waits for its own loads, the issuer for its MMAs, and the two
 // CTAs meet at a cluster barrier before they release the tensor memory.
@@ -41,13 +41,19 @@ using namespace tc;
 
 constexpr int PM = 256, HM = 128;       // pair tile rows, rows per CTA
 constexpr int BN = 256, HN = 128;       // pair tile columns, B columns staged per CTA
-constexpr int BK = 64, STAGES = 6;
+constexpr int BK = 64;
 constexpr int A_BYTES = HM * BK * 2;    // 16 KB
 constexpr int B_BYTES = HN * BK * 2;    // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_BYTES = 32 * 128;     // per epilogue warp: 32 rows x 64 bf16
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_BYTES + 1024;
-constexpr int NUM_THREADS = 224;
+// EW epilogue warps (4: each owns a TMEM lane quarter and all 256 columns; 8: two per lane
+// quarter, 128 columns each); the pipeline gets the stages that fit beside their staging.
+template <int EW> struct PairCfg {
+  static constexpr int STAGES = EW == 4 ? 6 : 5;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * EPI_BYTES + 1024;
+  static constexpr int THREADS = 32 * (3 + EW);
+  static constexpr int RELAY = 2 + EW;   // warp index of the relay
+};
 constexpr uint32_t TMEM_COLS = 512;     // two accumulator buffers of 256 fp32 columns
 constexpr int kMaxGroups = 1024 + 8;
 constexpr int SLAB = 64 * 128;          // one 64-element-wide, 64-row swizzled slab
@@ -164,15 +170,18 @@ __device__ __forceinline__ void issue_gather_half(const PairParams& p, const Til
 // one TMA tensor store; the TMEM load of the next chunk is in flight meanwhile.
 template <int MODE>
 __device__ __forceinline__ void epilogue_half(const PairParams& p, const TileCoord& tc, uint32_t rank,
-                                              int lg, uint32_t acc, uint8_t* stage, int lane) {
+                                              int lg, uint32_t acc, uint8_t* stage, int lane, int col0,
+                                              int ncols) {
   const GroupGeom& G = tc.G;
-  const int n0 = tc.ni * BN;
+  const int n0 = tc.ni * BN + col0;
+  acc += (uint32_t)col0;
   const int rowc = tc.mi * PM + HM * (int)rank + lg * 32;   // first row of this warp's 32
   if (rowc >= G.M) return;
   const CUtensorMap* om = G.shared ? &p.o1 : &p.o0;
   const int zc = G.shared ? G.s : G.e;
   const bool empty = G.K == 0;                              // dW of an expert without rows
-  const int nch = (min(BN, G.N - n0) + 63) / 64;
+  if (n0 >= G.N) return;
+  const int nch = (min(ncols, G.N - n0) + 63) / 64;
   uint4 pk[8];
   uint32_t u[64];
   if (!empty) {
@@ -213,9 +222,10 @@ __device__ __forceinline__ void epilogue_half(const PairParams& p, const TileCoo
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+template <int MODE, int EW>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS, 1)
     tc_pair_dw_kernel(const __grid_constant__ PairParams p) {
+  constexpr int STAGES = PairCfg<EW>::STAGES;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t land_bar[STAGES], full_bar[STAGES], empty_bar[STAGES];
   __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], final_bar;
@@ -242,7 +252,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull_bar[b]), 1);
-      mbar_init(smem_u32(&tempty_bar[b]), 8);   // 4 epilogue warps in each CTA
+      mbar_init(smem_u32(&tempty_bar[b]), 2 * EW);   // the epilogue warps of both CTAs
     }
     mbar_init(smem_u32(&final_bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -295,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     for (int s = 0; s < STAGES; ++s)
       if ((pending >> s) & 1u)
         mbar_wait_bounded(smem_u32(&land_bar[s]), (pend_par >> s) & 1u, nullptr, a.err, kWaitLimitNs);
-  } else if (warp == 6) {
+  } else if (warp == PairCfg<EW>::RELAY) {
     // ------------------------------------------------------------ relay (both CTAs)
     int stage = 0;
     uint32_t phase = 0;
@@ -376,6 +386,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue warps 2..5
     const int lg = warp & 3;              // TMEM lane quarter this warp may access
+    const int col0 = EW == 4 ? 0 : ((warp - 2) >> 2) * (BN / 2), ncols = EW == 4 ? BN : BN / 2;
     uint8_t* stage = smem + STAGES * STAGE_BYTES + (warp - 2) * EPI_BYTES;
     int it = 0;
     for (int tile = pair; tile < total; tile += npairs, ++it) {
@@ -386,7 +397,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (!__all_sync(0xffffffffu, got)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
       tc_fence_after();
       const uint32_t acc = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(b * BN);
-      epilogue_half<MODE>(p, tc, rank, lg, acc, stage, lane);
+      epilogue_half<MODE>(p, tc, rank, lg, acc, stage, lane, col0, ncols);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(peer_addr(smem_u32(&tempty_bar[b]), 0));
@@ -402,27 +413,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <int MODE>
-int launch_pair(PairParams& p, int num_sms, cudaStream_t st) {
-  static int clusters[2] = {0, 0};  // per mode: co-resident pairs of the persistent grid
-  int& nc = clusters[MODE == DW13 ? 1 : 0];
-  if (nc == 0) {
-    if (cudaFuncSetAttribute(tc_pair_dw_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int MODE, int EW>
+int launch_pair_ew(PairParams& p, int num_sms, cudaStream_t st) {
+  constexpr int SMEM_BYTES = PairCfg<EW>::SMEM_BYTES, THREADS = PairCfg<EW>::THREADS;
+  static int occ = 0;  // pairs that can be resident at once
+  if (occ == 0) {
+    if (cudaFuncSetAttribute(tc_pair_dw_kernel<MODE, EW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES) != cudaSuccess)
       return MOE_ERR_CUDA;
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3((unsigned)(num_sms & ~1));
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_pair_dw_kernel<MODE>, &cfg) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, tc_pair_dw_kernel<MODE, EW>, &cfg) != cudaSuccess || n <= 0)
       return MOE_ERR_CUDA;
-    nc = n < num_sms / 2 ? n : num_sms / 2;
+    occ = n;
   }
+  const int nc = occ < num_sms / 2 ? occ : num_sms / 2;
   TraceScope ts(MODE == DW13 ? TP_GEMM_DW13 : TP_GEMM_DW2, st);
-  tc_pair_dw_kernel<MODE><<<2 * nc, NUM_THREADS, SMEM_BYTES, st>>>(p);
+  tc_pair_dw_kernel<MODE, EW><<<2 * nc, THREADS, SMEM_BYTES, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;
+}
+
+// dW13 (2f = 4096 output rows, 5.0 vs 5.2 ms measured) takes eight epilogue warps and five
+// stages; dW2 (2.57 vs 2.60 ms) four warps and six stages.
+template <int MODE>
+int launch_pair(PairParams& p, int num_sms, cudaStream_t st) {
+  return MODE == DW13 ? launch_pair_ew<MODE, 8>(p, num_sms, st) : launch_pair_ew<MODE, 4>(p, num_sms, st);
 }
 
 }  // namespace
