@@ -182,3 +182,36 @@ def test_layer_at_the_expert_and_topk_limits(case):
     else:
         cfg = shrink("tiny_fp32", T=333, d=64, E=1024, k=32, f=64)
     check_layer(make_workload(cfg), bwd=True)
+
+
+def test_layer_step_replays_from_a_cuda_graph():
+    """The whole forward + backward is asynchronous on one stream with no host wait, so it
+    can be captured once in a CUDA graph and replayed: the replay gives the eager results bit
+    for bit (after the first eager call has set up the kernels' attributes)."""
+    from dropless_token_routing_gb300.api import LayerParams, MoELayer
+    w = make_workload(shrink("pangu_bf16", T=640, d=512, E=16, k=4, f=256, f_s=256))
+    c, dev = w.cfg, "cuda"
+    to = lambda t: None if t is None else t.to(dev)  # noqa: E731
+    params = LayerParams(w13=to(w.w13), w2=to(w.w2), w_r=to(w.w_r), bias=to(w.bias),
+                         ws13=to(w.ws13), ws2=to(w.ws2))
+    layer = MoELayer(params, c["T"], c["d"], c["E"], c["k"], c["f"], c["S"], c["f_s"], torch.bfloat16)
+    x, dy = to(w.x), to(w.dy)
+    y0 = layer.forward(x).clone()
+    g0 = {k_: v.clone() for k_, v in layer.backward(dy).items() if v is not None}
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        for t in list(layer.grads.values()) + [layer.y]:
+            if t is not None:
+                t.zero_()
+        with torch.cuda.graph(graph, stream=s):
+            layer.forward(x, stream=s)
+            layer.backward(dy, stream=s)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(layer.y, y0)
+    for k_, v in g0.items():
+        assert torch.equal(layer.grads[k_], v), k_
