@@ -80,7 +80,7 @@ template <int MODE> struct ModeTraits {
 
 // ------------------------------------------------------------------ producer: TMA issue
 // `gather`: the routed A tile is gathered row by row by the whole producer warp instead
-// (issue_gather_a), so it is skipped here.
+// (tma_gather4 in the producer loop), so it is skipped here.
 template <int MODE>
 __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCoord& tc, int kb,
                                                  uint32_t a_s, uint32_t b_s, uint32_t bar, bool gather) {
