@@ -215,3 +215,37 @@ def test_layer_step_replays_from_a_cuda_graph():
     assert torch.equal(layer.y, y0)
     for k_, v in g0.items():
         assert torch.equal(layer.grads[k_], v), k_
+
+
+# ---------------------------------------------------------------- randomised shapes
+def _random_shapes(n, seed):
+    import random
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        bf16 = i % 3 != 2
+        unit = 64 if bf16 else 8
+        E = rng.choice([1, 2, 3, 7, 16, 33, 64, 100, 257])
+        k = rng.randint(1, min(E, 32, 9))
+        S = rng.choice([0, 0, 1, 2])
+        cfg = dict(T=rng.choice([1, 5, 63, 64, 65, 200, 511, 700]), d=unit * rng.randint(1, 12),
+                   E=E, k=k, f=unit * rng.randint(1, 8), S=S,
+                   f_s=unit * rng.randint(1, 6) if S else 0)
+        base = "pangu_bf16" if bf16 else "tiny_fp32"
+        # the variants: dropless copies, drop-and-pad at a random capacity, fused row gathers
+        variant = rng.choice(["copy", "copy", "capacity", "gather"]) if bf16 else rng.choice(["copy", "capacity"])
+        cap = max(1, int(cfg["T"] * k / E * rng.choice([0.5, 1.0, 1.5]))) if variant == "capacity" else 0
+        out.append((base, cfg, cap, 1 if variant == "gather" else 0))
+    return out
+
+
+@pytest.mark.parametrize("base,over,capacity,rearrange", _random_shapes(24, 2027))
+def test_layer_on_random_shapes(base, over, capacity, rearrange):
+    """Seeded random shapes (ragged everything: T from 1 to 700, d and f at any multiple of the
+    vector unit, E up to 257, k up to 9, 0-2 shared experts, both dtypes), in the dropless,
+    drop-and-pad and fused-gather forms, each against the oracle at the usual bars."""
+    from layer_check import check_layer
+    cfg = shrink(base, **over)
+    if cfg["S"] == 0:
+        cfg["f_s"] = 0
+    check_layer(make_workload(cfg), bwd=True, capacity=capacity, rearrange=rearrange)
