@@ -202,3 +202,77 @@ def test_router_dw_identity(run):
     ref = w.x.double().T @ g["dlogits"].double()
     got = g["dw_r"].double()
     assert (torch.linalg.norm(got - ref) / torch.linalg.norm(ref)).item() <= 1e-5
+
+
+# ---------------------------------------------------------------- drop-and-pad at full size
+@pytest.fixture(scope="module")
+def run_capacity():
+    """The Pangu-shaped workload in the drop-and-pad variant at capacity factor 1.25, the
+    configuration bench.py times next to the dropless step."""
+    import math
+    from dropless_token_routing_gb300.api import LayerParams, MoELayer, get_device_error
+    cfg = dict(CONFIGS["pangu_bf16"], name="pangu_bf16")
+    C = math.ceil(1.25 * cfg["T"] * cfg["k"] / cfg["E"])
+    w = make_workload(cfg, device="cuda")
+    params = LayerParams(w13=w.w13, w2=w.w2, w_r=w.w_r, bias=w.bias, ws13=w.ws13, ws2=w.ws2)
+    layer = MoELayer(params, cfg["T"], cfg["d"], cfg["E"], cfg["k"], cfg["f"], cfg["S"], cfg["f_s"],
+                     torch.bfloat16, capacity=C)
+    layer.alloc_grads(with_dlogits=True)
+    layer.forward(w.x)
+    layer.backward(w.dy)
+    torch.cuda.synchronize()
+    assert get_device_error(layer.ws) == 0
+    yield cfg, C, w, layer
+    del layer, w
+    torch.cuda.empty_cache()
+
+
+def test_capacity_fullsize_permutation_and_sampled_tokens(run_capacity):
+    cfg, C, w, layer = run_capacity
+    s, g = layer.saved, layer.grads
+    k, f, d, E, S = cfg["k"], cfg["f"], cfg["d"], cfg["E"], cfg["S"]
+    idx, gate = _routing(cfg, w, layer)
+    assert np.array_equal(s["topk_idx"].cpu().numpy(), idx)
+    dest, row_src = O.capacity_permutation(idx, E, C)
+    assert np.array_equal(s["dest"].cpu().numpy(), dest)
+    assert np.array_equal(s["row_src"].cpu().numpy(), row_src)
+    assert np.array_equal(s["offsets"].cpu().numpy(), np.arange(E + 1) * C)
+    assert (dest < 0).any() and (row_src < 0).any()      # overflow dropped, short experts padded
+    pad = torch.as_tensor(row_src < 0).cuda()
+    assert not s["x_perm"][pad].any() and not s["w_perm"][pad].any()
+    kept = torch.as_tensor(row_src >= 0).cuda()
+    assert torch.equal(s["x_perm"][kept], w.x[s["row_src"][kept].long()])
+    # sampled tokens: only the kept copies contribute
+    toks = _sample_tokens("pangu_bf16", cfg, w, idx)
+    x, dy = _f64(w.x[toks]), _f64(w.dy[toks])
+    y_ref = np.zeros((len(toks), d))
+    dx_ref = np.zeros((len(toks), d))
+    dgate = np.zeros((len(toks), k))
+    for r, t in enumerate(toks):
+        for j in range(k):
+            if dest[t * k + j] < 0:
+                continue
+            e = int(idx[t, j])
+            W13, W2 = _f64(w.w13[e]), _f64(w.w2[e])
+            Z, H, Y = O.swiglu_rows(x[r:r + 1], W13, W2)
+            y_ref[r] += gate[t, j] * Y[0]
+            D = dy[r:r + 1] @ W2
+            dgate[r, j] = float(np.sum(D * H))
+            a, b = Z[:, :f], Z[:, f:]
+            dz = np.concatenate([gate[t, j] * D * b * O.silu_grad(a), gate[t, j] * D * O.silu(a)], 1)
+            dx_ref[r] += (dz @ W13)[0]
+    for s_ in range(S):
+        W13, W2 = _f64(w.ws13[s_]), _f64(w.ws2[s_])
+        fs = W13.shape[0] // 2
+        Z, H, Y = O.swiglu_rows(x, W13, W2)
+        y_ref += Y
+        D = dy @ W2
+        a, b = Z[:, :fs], Z[:, fs:]
+        dx_ref += np.concatenate([D * b * O.silu_grad(a), D * O.silu(a)], 1) @ W13
+    dl = O.router_backward(gate[toks], dgate)
+    dscores = np.zeros((len(toks), E))
+    np.put_along_axis(dscores, idx[toks], dl, axis=1)
+    dx_ref += dscores @ _f64(w.w_r).T
+    assert _rel(_f64(layer.y[toks]), y_ref) <= TOL
+    assert _rel(_f64(g["dx"][toks]), dx_ref) <= TOL
+    assert _rel(_f64(g["dlogits"][toks]), dscores) <= TOL
