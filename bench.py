@@ -85,6 +85,50 @@ def algorithmic_work(cfg):
     return flops, bytes_
 
 
+def group_roofline(cfg, counts, peaks):
+    """Per-group roofline of each grouped product: the sum over groups (the routed experts
+    with their n_e token copies, then the shared experts over all T tokens) of
+    max(flops_g / P, bytes_g / BW), in ms. A group below the ridge (n_e < P / BW in
+    flop per weight byte) is bound by streaming its weight (or, for the dW products,
+    writing its gradient) once; a group above it by the tensor cores. bytes_g counts the
+    weight (or gradient) of the group once plus its activation rows read and written."""
+    d, f, fs, S, T = cfg["d"], cfg["f"], cfg["f_s"], cfg["S"], cfg["T"]
+    es = 4 if cfg["dtype"] == "f32" else 2
+    P = peaks["bf16_tflops_sustained"] * 1e12
+    BW = peaks["hbm_gbs"] * 1e9
+    groups = [(n, f) for n in counts] + [(T, fs)] * S
+
+    def work(phase, n, w):
+        wgt = d * w * es                       # one of the three d x w matrices
+        if phase == "gemm_fwd1":               # x rows -> Z [n, 2w], h [n, w]
+            return 4.0 * d * w * n, 2 * wgt + es * n * (d + 3 * w)
+        if phase == "gemm_fwd2":               # h -> y_perm
+            return 2.0 * d * w * n, wgt + es * n * (w + d)
+        if phase == "gemm_bwd2t":              # dY rows, Z -> dz [n, 2w], hw [n, w], dgate
+            return 2.0 * d * w * n, wgt + es * n * (d + 5 * w) + 4 * n
+        if phase == "gemm_bwd1t":              # dz -> dx_perm
+            return 4.0 * d * w * n, 2 * wgt + es * n * (2 * w + d)
+        if phase == "gemm_dw2":                # dY rows, hw -> dW2 written
+            return 2.0 * d * w * n, wgt + es * n * (d + w)
+        if phase == "gemm_dw13":               # dz, x rows -> dW13 written
+            return 4.0 * d * w * n, 2 * wgt + es * n * (2 * w + d)
+        raise KeyError(phase)
+
+    out = {}
+    for phase in ("gemm_fwd1", "gemm_fwd2", "gemm_bwd2t", "gemm_bwd1t", "gemm_dw2", "gemm_dw13"):
+        per_group = 0.0
+        fl = by = 0.0
+        for n, w in groups:
+            a, b = work(phase, n, w)
+            per_group += max(a / P, b / BW)
+            fl += a
+            by += b
+        # the looser bound of the whole launch, every group overlapped with every other
+        out[phase] = {"per_group_ms": per_group * 1e3, "whole_launch_ms": max(fl / P, by / BW) * 1e3,
+                      "bytes": by}
+    return out
+
+
 def dw_write_bytes(cfg):
     """Bytes of dW written per launch by the two dW products (bf16 or fp32 gradients)."""
     es = 4 if cfg["dtype"] == "f32" else 2
@@ -551,6 +595,15 @@ def main():
     launches = sum(v[0] for v in trace.values())
 
     cnt = layer.saved["counts"].cpu().tolist()
+    groof = group_roofline(cfg, cnt, peaks)
+    for name, g in groof.items():
+        if name in kernels:
+            ms = kernels[name]["ms_per_step"]
+            kernels[name]["group_roofline"] = {
+                "per_group_ms": round(g["per_group_ms"], 4), "frac": round(g["per_group_ms"] / ms, 3),
+                "whole_launch_ms": round(g["whole_launch_ms"], 4),
+                "frac_whole_launch": round(g["whole_launch_ms"] / ms, 3)}
+    groof_ms = sum(g["per_group_ms"] for n_, g in groof.items() if n_ in trace)
     rows = sum(cnt) + cfg["S"] * T
     padded = sum(-(-c // 128) * 128 for c in cnt) + cfg["S"] * (-(-T // 128) * 128)
     routing_stats = {"max_expert_rows": max(cnt), "empty_experts": sum(1 for c in cnt if c == 0),
@@ -562,7 +615,9 @@ def main():
             "roofline": roof, "gpu_launches": launches, "e2e": e2e, "clocks": clocks,
             "grouped_gemm": {"tflops": round(gemm_flops / (gemm_ms / 1e3) / 1e12, 1),
                              "frac_of_dense_peak": round(gemm_flops / (gemm_ms / 1e3) / 1e12 /
-                                                         peaks["bf16_tflops_sustained"], 3)},
+                                                         peaks["bf16_tflops_sustained"], 3),
+                             "per_group_roofline_ms": round(groof_ms, 3),
+                             "frac_of_per_group_roofline": round(groof_ms / gemm_ms, 3) if gemm_ms else None},
             "routing": routing_stats, "kernels": kernels}
     if not args.no_cpu_baseline and world == 1:
         logits32 = (li if li is not None else layer.saved["logits"]).cpu().numpy()

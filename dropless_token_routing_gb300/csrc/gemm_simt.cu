@@ -10,7 +10,6 @@ namespace moe {
 namespace {
 
 constexpr int SBM = 32, SBN = 64, SBK = 32, STHREADS = 256;
-constexpr int kMaxGroups = 1024 + 8;
 
 template <int MODE> struct SimtOps {
   static constexpr bool a_mn = (MODE == DW2 || MODE == DW13);
@@ -92,18 +91,18 @@ __global__ void __launch_bounds__(STHREADS) simt_grouped_kernel(const GroupedArg
   __shared__ float As[SBK][SBM + 1];
   __shared__ float Bs[SBK][SBN + 1];
   __shared__ float red[SBM][SBN + 1];
-  __shared__ int tile_start[kMaxGroups + 1];
+  __shared__ TileSched sched;
   __shared__ int warp_sums[32];
   __shared__ int s_off[1024 + 1];
 
   const int bn_eff = (MODE == FWD1) ? SBN / 2 : SBN;
-  build_tile_starts(a, MODE, SBM, bn_eff, tile_start, warp_sums, s_off);
+  build_tile_starts(a, MODE, SBM, bn_eff, sched, warp_sums, s_off);
   const int ng = num_groups(MODE, a.E, a.S);
-  const int total = tile_start[ng];
+  const int total = sched_total(sched, ng);
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
 
   for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, SBM, s_off);
+    const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, SBM, s_off);
     const GroupGeom& G = tc.G;
     const int m0 = tc.mi * SBM, n0 = tc.ni * bn_eff;
     const int fw = G.shared ? a.f_s : a.f;

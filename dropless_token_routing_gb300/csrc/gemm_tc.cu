@@ -31,7 +31,6 @@ constexpr int EPI_STAGE_BYTES = 5120;        // per epilogue warp, a multiple of
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_STAGE_BYTES + 1024;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int kMaxGroups = 1024 + 8;
 constexpr int SLAB = 64 * 128;                // one 64-element-wide, 64-row swizzled slab
 
 using namespace tc;
@@ -356,7 +355,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
   __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], final_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
-  __shared__ int tile_start[kMaxGroups + 1];
+  __shared__ TileSched sched;
   __shared__ int warp_sums[32];
   __shared__ int s_off[1024 + 1];
 
@@ -387,11 +386,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     tc_fence_before();
   }
-  build_tile_starts(a, MODE, BM, TR::bn_eff, tile_start, warp_sums, s_off);  // ends with __syncthreads
+  build_tile_starts(a, MODE, BM, TR::bn_eff, sched, warp_sums, s_off);  // ends with __syncthreads
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
   const int ng = num_groups(MODE, a.E, a.S);
-  const int total = tile_start[ng];
+  const int total = sched_total(sched, ng);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -401,7 +400,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     uint32_t pend_par = 0;   // parity of the phase that load completes, per stage
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM, s_off);
+      const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, BM, s_off);
       const int nkb = (tc.G.K + BK - 1) / BK;
       // fused rearrangement: lane j gathers tile rows 4j..4j+3 (rows past the segment repeat
       // its first row; they are computed but never stored)
@@ -446,7 +445,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
       bool issued = false, ok = true;
       int it = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-        const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM, s_off);
+        const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, BM, s_off);
         const int nkb = (tc.G.K + BK - 1) / BK;
         const int b = it & 1;
         if (!mbar_wait_bounded(smem_u32(&tempty_bar[b]), ((it >> 1) & 1) ^ 1, &abort_flag, a.err,
@@ -485,7 +484,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     uint8_t* stage = smem + STAGES * STAGE_BYTES + (warp - 2) * EPI_STAGE_BYTES;
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, BM, s_off);
+      const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, BM, s_off);
       const int b = it & 1;
       const bool got = mbar_wait_bounded(smem_u32(&tfull_bar[b]), (it >> 1) & 1, &abort_flag,
                                          a.err, kWaitLimitNs);

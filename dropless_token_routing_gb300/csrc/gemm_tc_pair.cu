@@ -55,7 +55,6 @@ template <int EW> struct PairCfg {
   static constexpr int RELAY = 2 + EW;   // warp index of the relay
 };
 constexpr uint32_t TMEM_COLS = 512;     // two accumulator buffers of 256 fp32 columns
-constexpr int kMaxGroups = 1024 + 8;
 constexpr int SLAB = 64 * 128;          // one 64-element-wide, 64-row swizzled slab
 
 struct PairParams {
@@ -231,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
   __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], final_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
-  __shared__ int tile_start[kMaxGroups + 1];
+  __shared__ TileSched sched;
   __shared__ int warp_sums[32];
   __shared__ int s_off[1024 + 1];
 
@@ -266,12 +265,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     tc_fence_before();
   }
-  build_tile_starts(a, MODE, PM, BN, tile_start, warp_sums, s_off);  // ends with __syncthreads
+  build_tile_starts(a, MODE, PM, BN, sched, warp_sums, s_off);  // ends with __syncthreads
   cluster_sync_all();   // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
   const int ng = num_groups(MODE, a.E, a.S);
-  const int total = tile_start[ng];
+  const int total = sched_total(sched, ng);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -279,7 +278,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
     uint32_t phase = 0, pending = 0, pend_par = 0;
     bool ok = true;
     for (int tile = pair; tile < total && ok; tile += npairs) {
-      const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, PM, s_off);
+      const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, PM, s_off);
       const int nkb = (tc.G.K + BK - 1) / BK;
       const bool gather = a.gather_rows != nullptr && !tc.G.shared;
       for (int kb = 0; kb < nkb; ++kb) {
@@ -311,7 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
     uint32_t phase = 0;
     bool ok = true;
     for (int tile = pair; tile < total && ok; tile += npairs) {
-      const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, PM, s_off);
+      const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, PM, s_off);
       const int nkb = (tc.G.K + BK - 1) / BK;
       for (int kb = 0; kb < nkb; ++kb) {
         const bool got = mbar_wait_bounded(smem_u32(&land_bar[stage]), phase, &abort_flag, a.err,
@@ -343,7 +342,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
       bool issued = false, ok = true;
       int it = 0;
       for (int tile = pair; tile < total && ok; tile += npairs, ++it) {
-        const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, PM, s_off);
+        const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, PM, s_off);
         const int nkb = (tc.G.K + BK - 1) / BK;
         const int b = it & 1;
         if (!mbar_wait_bounded(smem_u32(&tempty_bar[b]), ((it >> 1) & 1) ^ 1, &abort_flag, a.err,
@@ -390,7 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
     uint8_t* stage = smem + STAGES * STAGE_BYTES + (warp - 2) * EPI_BYTES;
     int it = 0;
     for (int tile = pair; tile < total; tile += npairs, ++it) {
-      const TileCoord tc = decode_tile(a, MODE, tile_start, ng, tile, PM, s_off);
+      const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, PM, s_off);
       const int b = it & 1;
       const bool got = mbar_wait_bounded(smem_u32(&tfull_bar[b]), (it >> 1) & 1, &abort_flag, a.err,
                                          kWaitLimitNs);

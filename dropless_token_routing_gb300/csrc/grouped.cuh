@@ -112,31 +112,27 @@ __device__ __forceinline__ GroupGeom group_geom(const GroupedArgs& a, int mode, 
   return G;
 }
 
-// Copies the expert offsets into s_off[0..E] and scans the per-group tile counts into
-// tile_start[0..ng] (both shared memory). Every thread of the block must call it.
-// bn_eff = output columns one tile covers along N (for FWD1 this is gate columns: a tile
-// holds bn_eff gate and bn_eff up columns).
-__device__ __forceinline__ void build_tile_starts(const GroupedArgs& a, int mode, int bm,
-                                                  int bn_eff, int* tile_start, int* warp_sums,
-                                                  int* s_off) {
-  if (mode != ROUTER)
-    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = __ldg(a.offsets + i);
-  __syncthreads();
-  const int ng = num_groups(mode, a.E, a.S);
-  const int nt = blockDim.x;
-  const int per = (ng + nt - 1) / nt;
-  const int g0 = threadIdx.x * per;
-  int local = 0;
-  for (int i = 0; i < per; ++i) {
-    const int g = g0 + i;
-    if (g < ng) {
-      const GroupGeom G = group_geom(a, mode, g, s_off);
-      const int t = ((G.M + bm - 1) / bm) * ((G.N + bn_eff - 1) / bn_eff);
-      tile_start[g] = t;  // temporarily the count
-      local += t;
-    }
-  }
-  // exclusive scan of `local` across the block
+constexpr int kMaxGroups = 1024 + 8;   // routed experts (at most 1024) plus the shared ones
+
+// Groups with more rows than this reuse each weight tile over three or more 128-row M tiles
+// (or, in the dW products, reduce over more than four 64-deep K blocks): at the sustained
+// tensor rate against the HBM bandwidth their tiles are bound by the tensor cores, while
+// the tiles of smaller groups are bound by streaming the group's weight (or writing its
+// gradient). The schedule mixes the two kinds so that both units stay busy.
+constexpr int64_t kHeavyRows = 256;
+
+// Tile schedule of one grouped launch, built in shared memory by every CTA. The groups
+// are split into two streams, 0 (at most kHeavyRows rows, or every group where the launch
+// is not mixed) and 1 (more); start[s][g] is
+// the first tile of group g within stream s (groups of the other stream hold no tiles
+// there), start[s][ng] the stream's tile count.
+struct TileSched {
+  int start[2][kMaxGroups + 1];
+};
+
+// Exclusive block-wide scan of one int per thread; returns the thread's prefix.
+// Every thread of the block must call it.
+__device__ __forceinline__ int block_exclusive_scan(int local, int* warp_sums) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int inc = local;
 #pragma unroll
@@ -147,7 +143,7 @@ __device__ __forceinline__ void build_tile_starts(const GroupedArgs& a, int mode
   if (lane == 31) warp_sums[warp] = inc;
   __syncthreads();
   if (warp == 0) {
-    const int nw = (nt + 31) >> 5;
+    const int nw = (blockDim.x + 31) >> 5;
     int v = lane < nw ? warp_sums[lane] : 0;
     int vi = v;
 #pragma unroll
@@ -158,20 +154,68 @@ __device__ __forceinline__ void build_tile_starts(const GroupedArgs& a, int mode
     if (lane < nw) warp_sums[lane] = vi - v;
   }
   __syncthreads();
-  int run = warp_sums[warp] + inc - local;
+  const int r = warp_sums[warp] + inc - local;
+  __syncthreads();   // warp_sums is reused by the next scan
+  return r;
+}
+
+// Copies the expert offsets into s_off[0..E] and builds the tile schedule (both shared
+// memory). Every thread of the block must call it.
+// bn_eff = output columns one tile covers along N (for FWD1 this is gate columns: a tile
+// holds bn_eff gate and bn_eff up columns).
+__device__ __forceinline__ void build_tile_starts(const GroupedArgs& a, int mode, int bm,
+                                                  int bn_eff, TileSched& ts, int* warp_sums,
+                                                  int* s_off) {
+  if (mode != ROUTER)
+    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_off[i] = __ldg(a.offsets + i);
+  __syncthreads();
+  const int ng = num_groups(mode, a.E, a.S);
+  // measured per product: mixing shortens the products whose B operand is the expert
+  // weight read along the full hidden size or width (FWD1, FWD2, BWD1T) and lengthens
+  // BWD2T and the dW products, which keep the plain group order
+  const bool mixed = mode == FWD1 || mode == FWD2 || mode == BWD1T;
+  const int nt = blockDim.x;
+  const int per = (ng + nt - 1) / nt;
+  const int g0 = threadIdx.x * per;
+  int local[2] = {0, 0};
   for (int i = 0; i < per; ++i) {
     const int g = g0 + i;
     if (g < ng) {
-      const int t = tile_start[g];
-      tile_start[g] = run;
-      run += t;
+      const GroupGeom G = group_geom(a, mode, g, s_off);
+      const int t = ((G.M + bm - 1) / bm) * ((G.N + bn_eff - 1) / bn_eff);
+      const int s = (mixed && G.rows > kHeavyRows) ? 1 : 0;
+      ts.start[s][g] = t;      // temporarily the count
+      ts.start[s ^ 1][g] = 0;
+      local[s] += t;
     }
   }
-  if (threadIdx.x == nt - 1) tile_start[ng] = run;
+  int run[2];
+  run[0] = block_exclusive_scan(local[0], warp_sums);
+  run[1] = block_exclusive_scan(local[1], warp_sums);
+  for (int i = 0; i < per; ++i) {
+    const int g = g0 + i;
+    if (g < ng) {
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int t = ts.start[s][g];
+        ts.start[s][g] = run[s];
+        run[s] += t;
+      }
+    }
+  }
+  if (threadIdx.x == nt - 1) {
+    ts.start[0][ng] = run[0];
+    ts.start[1][ng] = run[1];
+  }
   __syncthreads();
 }
 
-// Group owning linear tile `tile` (tile_start is non-decreasing; empty groups are skipped).
+__device__ __forceinline__ int sched_total(const TileSched& ts, int ng) {
+  return ts.start[0][ng] + ts.start[1][ng];
+}
+
+// Group owning tile `tile` of one stream (tile_start is non-decreasing; groups with no
+// tiles in the stream are skipped).
 __device__ __forceinline__ int find_group(const int* tile_start, int ng, int tile) {
   int lo = 0, hi = ng;  // answer in [lo, hi)
   while (hi - lo > 1) {
@@ -186,14 +230,23 @@ struct TileCoord {
   int g, mi, ni;
 };
 
-// Tiles of a group are ordered N-tile major, M-tile minor, so that CTAs working at the same
-// time on one expert share its weight tile through L2.
-__device__ __forceinline__ TileCoord decode_tile(const GroupedArgs& a, int mode, const int* tile_start,
+// Linear tile -> (group, M tile, N tile). The two streams are merged in proportion: of
+// the first i tiles, floor(i * n0 / (n0 + n1)) come from stream 0, so every stretch of the
+// launch holds both kinds of tile. Within a stream the groups keep their order, and the
+// tiles of a group are ordered N-tile major, M-tile minor, so that CTAs working at the
+// same time on one expert share its weight tile through L2.
+__device__ __forceinline__ TileCoord decode_tile(const GroupedArgs& a, int mode, const TileSched& ts,
                                                  int ng, int tile, int bm, const int* s_off) {
+  const int n0 = ts.start[0][ng];
+  const long long tot = (long long)n0 + ts.start[1][ng];
+  const int lo = (int)((long long)tile * n0 / tot);
+  const int hi = (int)((long long)(tile + 1) * n0 / tot);
+  const int s = hi > lo ? 0 : 1;
+  const int j = s == 0 ? lo : tile - lo;
   TileCoord c;
-  c.g = find_group(tile_start, ng, tile);
+  c.g = find_group(ts.start[s], ng, j);
   c.G = group_geom(a, mode, c.g, s_off);
-  const int local = tile - tile_start[c.g];
+  const int local = j - ts.start[s][c.g];
   const int mt = (c.G.M + bm - 1) / bm;
   c.ni = local / mt;
   c.mi = local - c.ni * mt;
