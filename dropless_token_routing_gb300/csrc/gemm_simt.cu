@@ -98,11 +98,10 @@ __global__ void __launch_bounds__(STHREADS) simt_grouped_kernel(const GroupedArg
   const int bn_eff = (MODE == FWD1) ? SBN / 2 : SBN;
   build_tile_starts(a, MODE, SBM, bn_eff, sched, warp_sums, s_off);
   const int ng = num_groups(MODE, a.E, a.S);
-  const int total = sched_total(sched, ng);
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
 
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, SBM, s_off);
+  for (TileCursor cur(sched, ng, blockIdx.x, gridDim.x); cur.valid(); cur.advance()) {
+    const TileCoord tc = cur.coord(a, MODE, SBM, s_off);
     const GroupGeom& G = tc.G;
     const int m0 = tc.mi * SBM, n0 = tc.ni * bn_eff;
     const int fw = G.shared ? a.f_s : a.f;

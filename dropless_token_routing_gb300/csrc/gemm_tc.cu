@@ -390,7 +390,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
   const int ng = num_groups(MODE, a.E, a.S);
-  const int total = sched_total(sched, ng);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -399,8 +398,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     uint32_t pending = 0;    // stages whose latest load may still be in flight
     uint32_t pend_par = 0;   // parity of the phase that load completes, per stage
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, BM, s_off);
+    for (TileCursor cur(sched, ng, blockIdx.x, gridDim.x); cur.valid() && ok; cur.advance()) {
+      const TileCoord tc = cur.coord(a, MODE, BM, s_off);
       const int nkb = (tc.G.K + BK - 1) / BK;
       // fused rearrangement: lane j gathers tile rows 4j..4j+3 (rows past the segment repeat
       // its first row; they are computed but never stored)
@@ -444,8 +443,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
       uint32_t phase = 0;
       bool issued = false, ok = true;
       int it = 0;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-        const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, BM, s_off);
+      for (TileCursor cur(sched, ng, blockIdx.x, gridDim.x); cur.valid() && ok; cur.advance(), ++it) {
+        const TileCoord tc = cur.coord(a, MODE, BM, s_off);
         const int nkb = (tc.G.K + BK - 1) / BK;
         const int b = it & 1;
         if (!mbar_wait_bounded(smem_u32(&tempty_bar[b]), ((it >> 1) & 1) ^ 1, &abort_flag, a.err,
@@ -483,8 +482,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     const int r = lg * 32 + lane;         // tile row
     uint8_t* stage = smem + STAGES * STAGE_BYTES + (warp - 2) * EPI_STAGE_BYTES;
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const TileCoord tc = decode_tile(a, MODE, sched, ng, tile, BM, s_off);
+    for (TileCursor cur(sched, ng, blockIdx.x, gridDim.x); cur.valid(); cur.advance(), ++it) {
+      const TileCoord tc = cur.coord(a, MODE, BM, s_off);
       const int b = it & 1;
       const bool got = mbar_wait_bounded(smem_u32(&tfull_bar[b]), (it >> 1) & 1, &abort_flag,
                                          a.err, kWaitLimitNs);

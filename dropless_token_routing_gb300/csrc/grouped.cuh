@@ -210,47 +210,70 @@ __device__ __forceinline__ void build_tile_starts(const GroupedArgs& a, int mode
   __syncthreads();
 }
 
-__device__ __forceinline__ int sched_total(const TileSched& ts, int ng) {
-  return ts.start[0][ng] + ts.start[1][ng];
-}
-
-// Group owning tile `tile` of one stream (tile_start is non-decreasing; groups with no
-// tiles in the stream are skipped).
-__device__ __forceinline__ int find_group(const int* tile_start, int ng, int tile) {
-  int lo = 0, hi = ng;  // answer in [lo, hi)
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (tile_start[mid] <= tile) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
 struct TileCoord {
   GroupGeom G;
   int g, mi, ni;
 };
 
-// Linear tile -> (group, M tile, N tile). The two streams are merged in proportion: of
-// the first i tiles, floor(i * n0 / (n0 + n1)) come from stream 0, so every stretch of the
-// launch holds both kinds of tile. Within a stream the groups keep their order, and the
-// tiles of a group are ordered N-tile major, M-tile minor, so that CTAs working at the
-// same time on one expert share its weight tile through L2.
-__device__ __forceinline__ TileCoord decode_tile(const GroupedArgs& a, int mode, const TileSched& ts,
-                                                 int ng, int tile, int bm, const int* s_off) {
-  const int n0 = ts.start[0][ng];
-  const long long tot = (long long)n0 + ts.start[1][ng];
-  const int lo = (int)((long long)tile * n0 / tot);
-  const int hi = (int)((long long)(tile + 1) * n0 / tot);
-  const int s = hi > lo ? 0 : 1;
-  const int j = s == 0 ? lo : tile - lo;
-  TileCoord c;
-  c.g = find_group(ts.start[s], ng, j);
-  c.G = group_geom(a, mode, c.g, s_off);
-  const int local = j - ts.start[s][c.g];
-  const int mt = (c.G.M + bm - 1) / bm;
-  c.ni = local / mt;
-  c.mi = local - c.ni * mt;
-  return c;
-}
+// Walks one CTA's (or CTA pair's) tiles, first, first + stride, ..., through the schedule.
+// The two streams are merged in proportion: of the first i tiles, floor(i * n0 / (n0 + n1))
+// come from stream 0, so every stretch of the launch holds both kinds of tile. Within a
+// stream the groups keep their order, and the tiles of a group are ordered N-tile major,
+// M-tile minor, so that CTAs working at the same time on one expert share its weight tile
+// through L2. Each step costs a few integer operations: the merge position is carried as a
+// quotient and remainder, and the group of each stream only moves forward. (The issuing
+// threads of the short-K dW tiles cannot afford a search or a 64-bit division per tile.)
+struct TileCursor {
+  const int* st0;    // stream 0's group starts (shared memory)
+  const int* st1;
+  int ng, n0, stride;
+  long long tot;
+  int tile;
+  int q;             // floor(tile * n0 / tot)
+  long long r;       // tile * n0 - q * tot
+  int dq;            // floor(stride * n0 / tot)
+  long long dr;
+  int g0 = 0, g1 = 0;  // current group of each stream
+  int cached = -1;     // group whose geometry is in G
+  GroupGeom G;
+
+  __device__ __forceinline__ TileCursor(const TileSched& t, int ng_, int first, int stride_)
+      : st0(t.start[0]), st1(t.start[1]), ng(ng_), n0(t.start[0][ng_]), stride(stride_),
+        tot((long long)t.start[0][ng_] + t.start[1][ng_]), tile(first) {
+    const long long d = tot > 0 ? tot : 1;
+    q = (int)((long long)first * n0 / d);
+    r = (long long)first * n0 - (long long)q * d;
+    dq = (int)((long long)stride * n0 / d);
+    dr = (long long)stride * n0 - (long long)dq * d;
+  }
+  __device__ __forceinline__ bool valid() const { return tile < tot; }
+  __device__ __forceinline__ void advance() {
+    tile += stride;
+    q += dq;
+    r += dr;
+    if (r >= tot) { r -= tot; ++q; }
+  }
+  __device__ __forceinline__ TileCoord coord(const GroupedArgs& a, int mode, int bm, const int* s_off) {
+    // tile is stream 0's iff floor((tile + 1) n0 / tot) > floor(tile n0 / tot)
+    const bool s0 = r + n0 >= tot;
+    const int j = s0 ? q : tile - q;
+    const int* st = s0 ? st0 : st1;
+    int gg = s0 ? g0 : g1;
+    while (gg + 1 < ng && st[gg + 1] <= j) ++gg;
+    if (s0) g0 = gg; else g1 = gg;
+    if (gg != cached) {
+      G = group_geom(a, mode, gg, s_off);
+      cached = gg;
+    }
+    TileCoord c;
+    c.g = gg;
+    c.G = G;
+    const int local = j - st[gg];
+    const int mt = (G.M + bm - 1) / bm;
+    c.ni = local / mt;
+    c.mi = local - c.ni * mt;
+    return c;
+  }
+};
 
 }  // namespace moe
