@@ -48,13 +48,9 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_BYTES = 32 * 128;     // per epilogue warp: 32 rows x 64 bf16
 // EW epilogue warps (4: each owns a TMEM lane quarter and all 256 columns; 8: two per lane
 // quarter, 128 columns each); the pipeline gets the stages that fit beside their staging.
-#ifndef MOE_DW_STG
-#define MOE_DW_STG 1
-#endif
 template <int EW> struct PairCfg {
-  static constexpr int NSTG = MOE_DW_STG;   // staging buffers per epilogue warp
-  static constexpr int STAGES = (EW == 4 ? 6 : 5) - (NSTG > 1 ? 1 : 0);
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * NSTG * EPI_BYTES + 1024;
+  static constexpr int STAGES = EW == 4 ? 6 : 5;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * EPI_BYTES + 1024;
   static constexpr int THREADS = 32 * (3 + EW);
   static constexpr int RELAY = 2 + EW;   // warp index of the relay
 };
@@ -171,10 +167,10 @@ __device__ __forceinline__ void issue_gather_half(const PairParams& p, const Til
 // The warp owns 32 rows of this CTA's 128 x 256 half tile (its TMEM lane quarter). Each
 // 32 x 64 chunk is converted to bf16, staged in the 128-byte swizzled layout and written by
 // one TMA tensor store; the TMEM load of the next chunk is in flight meanwhile.
-template <int MODE, int NSTG>
+template <int MODE>
 __device__ __forceinline__ void epilogue_half(const PairParams& p, const TileCoord& tc, uint32_t rank,
                                               int lg, uint32_t acc, uint8_t* stage, int lane, int col0,
-                                              int ncols, int& sb) {
+                                              int ncols) {
   const GroupGeom& G = tc.G;
   const int n0 = tc.ni * BN + col0;
   acc += (uint32_t)col0;
@@ -210,17 +206,15 @@ __device__ __forceinline__ void epilogue_half(const PairParams& p, const TileCoo
 #pragma unroll
       for (int q = 0; q < 8; ++q) pk[q] = make_uint4(0u, 0u, 0u, 0u);
     }
-    uint8_t* buf = stage + (sb % NSTG) * EPI_BYTES;
-    ++sb;
-    if (lane == 0) bulk_wait_read<NSTG - 1>();   // the store that last used buf has left it
+    if (lane == 0) bulk_wait_read0();      // the previous store has left the buffer
     __syncwarp();
-    uint4* srow = reinterpret_cast<uint4*>(buf + lane * 128);
+    uint4* srow = reinterpret_cast<uint4*>(stage + lane * 128);
 #pragma unroll
     for (int q = 0; q < 8; ++q) srow[q ^ (lane & 7)] = pk[q];
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) {
-      tma_store3d(om, smem_u32(buf), n0 + c, rowc, zc);
+      tma_store3d(om, smem_u32(stage), n0 + c, rowc, zc);
       bulk_commit();
     }
   }
@@ -391,9 +385,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
     // ------------------------------------------------------------ epilogue warps 2..5
     const int lg = warp & 3;              // TMEM lane quarter this warp may access
     const int col0 = EW == 4 ? 0 : ((warp - 2) >> 2) * (BN / 2), ncols = EW == 4 ? BN : BN / 2;
-    constexpr int NSTG = PairCfg<EW>::NSTG;
-    uint8_t* stage = smem + STAGES * STAGE_BYTES + (warp - 2) * NSTG * EPI_BYTES;
-    int it = 0, sb = 0;
+    uint8_t* stage = smem + STAGES * STAGE_BYTES + (warp - 2) * EPI_BYTES;
+    int it = 0;
     for (TileCursor cur(sched, ng, pair, npairs); cur.valid(); cur.advance(), ++it) {
       const TileCoord tc = cur.coord(a, MODE, PM, s_off);
       const int b = it & 1;
@@ -402,7 +395,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
       if (!__all_sync(0xffffffffu, got)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
       tc_fence_after();
       const uint32_t acc = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(b * BN);
-      epilogue_half<MODE, NSTG>(p, tc, rank, lg, acc, stage, lane, col0, ncols, sb);
+      epilogue_half<MODE>(p, tc, rank, lg, acc, stage, lane, col0, ncols);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(peer_addr(smem_u32(&tempty_bar[b]), 0));
