@@ -492,28 +492,70 @@ __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int
 // Router dW: dW_r[:, e] = sum over the copies routed to e of dl * x[token]. Deterministic:
 // each expert's rows are cut into kDwrSplit fixed slices, each slice summed in row order,
 // then the slices are summed in slice order.
+// 16 bytes of x as fp32: 8 bf16 or 4 fp32 columns.
+__device__ __forceinline__ void vec16_to_f32(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ void vec16_to_f32(const uint4& u, float (&f)[4]) {
+  f[0] = __uint_as_float(u.x);
+  f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z);
+  f[3] = __uint_as_float(u.w);
+}
+
+// Each thread owns 16 bytes of columns; the rows of its slice are fetched four at a time
+// (indices, then the x vectors) and accumulated one by one in row order.
 template <typename TX>
 __global__ void __launch_bounds__(256) dwr_partial_kernel(const TX* __restrict__ x,
                                                           const int32_t* __restrict__ row_src,
                                                           const float* __restrict__ dl_perm,
                                                           const int32_t* __restrict__ offsets, int d,
                                                           int E, float* __restrict__ part) {
+  constexpr int V = 16 / sizeof(TX);
   const int e = blockIdx.x / kDwrSplit, sl = blockIdx.x % kDwrSplit;
   const int64_t lo = offsets[e], n = offsets[e + 1] - lo;
   const int64_t r0 = lo + n * sl / kDwrSplit, r1 = lo + n * (sl + 1) / kDwrSplit;
-  const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  const int c = (blockIdx.y * blockDim.x + threadIdx.x) * V;
   if (c >= d) return;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int64_t r = r0; r < r1; ++r) {
-    const int64_t t = row_src[r];
-    const float g = dl_perm[r];
-    const TX* xr = x + t * d + c;
+  float acc[V];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = fmaf(g, to_f32(xr[i]), acc[i]);
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
+  int64_t r = r0;
+  for (; r + 4 <= r1; r += 4) {
+    int64_t t[4];
+    float g[4];
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      t[j] = row_src[r + j];
+      g[j] = dl_perm[r + j];
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = __ldg(reinterpret_cast<const uint4*>(x + t[j] * d + c));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float f[V];
+      vec16_to_f32(v[j], f);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = fmaf(g[j], f[i], acc[i]);
+    }
   }
-  float* out = part + ((int64_t)sl * E + e) * d + c;
+  for (; r < r1; ++r) {
+    float f[V];
+    vec16_to_f32(__ldg(reinterpret_cast<const uint4*>(x + (int64_t)row_src[r] * d + c)), f);
+    const float g = dl_perm[r];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) out[i] = acc[i];
+    for (int i = 0; i < V; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+  }
+  float4* out = reinterpret_cast<float4*>(part + ((int64_t)sl * E + e) * d + c);
+#pragma unroll
+  for (int i = 0; i < V / 4; ++i) out[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
 }
 
 // dw_r[c][e] = sum_sl part[sl][e][c] (slice order), through a 32x32 transpose tile.
@@ -693,7 +735,8 @@ cudaError_t launch_transpose_f32(const float* in, int rows, int cols, float* out
 cudaError_t launch_dwr(const void* x, const int32_t* row_src, const float* dl_perm,
                        const int32_t* offsets, const moe_dims& dm, float* part, float* dw_r,
                        cudaStream_t st) {
-  const dim3 g1(dm.E * kDwrSplit, (dm.d + 1023) / 1024), b1(256);
+  const int cols_per_block = 256 * (dm.dtype == MOE_F32 ? 4 : 8);
+  const dim3 g1(dm.E * kDwrSplit, (dm.d + cols_per_block - 1) / cols_per_block), b1(256);
   {
   TraceScope ts(TP_DWR, st);
   if (dm.dtype == MOE_F32)
