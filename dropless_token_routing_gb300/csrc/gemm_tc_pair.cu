@@ -364,7 +364,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
                       (kb | kk) != 0 ? 1u : 0u);
           }
           issued = true;
-          umma_commit_mc(smem_u32(&empty_bar[stage]), 0x3);
+          // the tile's last stage is released by the epilogue once the accumulator is full:
+          // a commit straight after another one stalls the tensor pipe
+          if (kb + 1 < nkb) umma_commit_mc(smem_u32(&empty_bar[stage]), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -386,13 +388,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
     const int lg = warp & 3;              // TMEM lane quarter this warp may access
     const int col0 = EW == 4 ? 0 : ((warp - 2) >> 2) * (BN / 2), ncols = EW == 4 ? BN : BN / 2;
     uint8_t* stage = smem + STAGES * STAGE_BYTES + (warp - 2) * EPI_BYTES;
-    int it = 0;
+    int it = 0, kblocks = 0;   // tiles and K blocks seen so far
     for (TileCursor cur(sched, ng, pair, npairs); cur.valid(); cur.advance(), ++it) {
       const TileCoord tc = cur.coord(a, MODE, PM, s_off);
       const int b = it & 1;
       const bool got = mbar_wait_bounded(smem_u32(&tfull_bar[b]), (it >> 1) & 1, &abort_flag, a.err,
                                          kWaitLimitNs);
       if (!__all_sync(0xffffffffu, got)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
+      // the accumulator is full, so every MMA of the tile has read its operands: release the
+      // stage of the tile's last K block in this CTA (the issuer commits the others)
+      const int nkb = (tc.G.K + BK - 1) / BK;
+      if (warp == 2 && lane == 0 && nkb > 0) mbar_arrive(smem_u32(&empty_bar[(kblocks + nkb - 1) % STAGES]));
+      kblocks += nkb;
       tc_fence_after();
       const uint32_t acc = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(b * BN);
       epilogue_half<MODE>(p, tc, rank, lg, acc, stage, lane, col0, ncols);
