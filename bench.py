@@ -40,8 +40,8 @@ NCU_TRAFFIC = {
     # ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum (one pass)
     # on the default workload, one launch after warm-up; see profiles/gemm_dw13_pangu_bf16.md.
     # Applies only while the kernel's source file is unchanged since the capture.
-    "gemm_dw13": {"src": "gemm_tc_pair.cu", "bytes_per_launch": 3599732992 + 16168961792,
-                  "src_sha256": "72025f869a1c31e2bd2c9f74f611983d33f4fdcdd5ddddfe90f7a587ee30de11"},
+    "gemm_dw13": {"src": "gemm_tc_pair.cu", "bytes_per_launch": 3434076416 + 16167639296,
+                  "src_sha256": "b156194b67bdbb1cc14e007ad3d485fb219b67ccf2577fd7f0ec22b172f4dbc6"},
 }
 
 
