@@ -40,7 +40,8 @@ NCU_TRAFFIC = {
     # ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum (one pass)
     # on the default workload, one launch after warm-up; see profiles/gemm_dw13_pangu_bf16.md.
     # Applies only while the kernel's source file is unchanged since the capture.
-    "gemm_dw13": {"src": "gemm_tc_pair.cu", "bytes_per_launch": 3434076416 + 16167639296,
+    "gemm_dw13": {"src": "gemm_tc_pair.cu", "workload": "pangu_bf16",
+                  "bytes_per_launch": 3434076416 + 16167639296,
                   "src_sha256": "b156194b67bdbb1cc14e007ad3d485fb219b67ccf2577fd7f0ec22b172f4dbc6"},
 }
 
@@ -547,7 +548,8 @@ def main():
     per = dms / dl
     traffic = None
     tr = NCU_TRAFFIC.get(dom)
-    if tr and tr.get("bytes_per_launch"):
+    # the captured bytes hold only for the workload they were captured on
+    if tr and tr.get("bytes_per_launch") and tr.get("workload") == cfg["name"]:
         src = os.path.join(ROOT, "dropless_token_routing_gb300", "csrc", tr["src"])
         if tr.get("src_sha256") == _sha(src):
             traffic = tr["bytes_per_launch"]
