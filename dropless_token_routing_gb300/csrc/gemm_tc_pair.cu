@@ -15,17 +15,18 @@
 // Roles in each CTA of the pair (3 + EW warps, EW = 4 or 8 epilogue warps):
 //   warp 0      TMA producer: this CTA's A and B halves into the 6- (or 5-) stage ring; the
 //               bytes complete on this CTA's land_bar
-//   warp 1      TMEM owner (the pair allocates together); in the even CTA the lane-0 thread
-//               issues the MMAs of the pair
+//   warp 1      TMEM owner (the pair allocates together); in the even CTA its lane-0
+//               thread issues the MMAs of the even tiles (accumulator 0)
 //   warps 2..   epilogue: TMEM -> bf16 -> 128-byte swizzled staging -> TMA tensor store
-//   last warp   relay: waits until this CTA's K block has landed, zeroes the A rows past a
-//               ragged expert segment, then arrives on the even CTA's full_bar, which
-//               therefore completes once both halves of the K block are in place
-// The issuer's commits arrive on the stage and accumulator barriers of both CTAs
+//   warp 2+EW   relay: waits until this CTA's K block has landed, zeroes the A rows past a
+//               ragged expert segment, then arrives on the even CTA's full_bar of the
+//               tile's issuer, which therefore completes once both halves are in place
+//   warp 3+EW   in the even CTA, lane 0 issues the MMAs of the odd tiles (accumulator 1)
+// The issuers' commits arrive on the stage and accumulator barriers of both CTAs
 // (multicast); each epilogue warp of either CTA frees an accumulator buffer by arriving on
 // the even CTA's tempty_bar (2 * EW arrivals).
 // Every mbarrier wait is bounded (1 s). On expiry the CTA records MOE_ERR_DEVICE_TIMEOUT and
-// winds down: its producer waits for its own loads, the issuer for its MMAs, and the two
+// winds down: its producer waits for its own loads, the issuers for their MMAs, and the two
 // CTAs meet at a cluster barrier before they release the tensor memory.
 #include <cuda.h>
 
@@ -51,8 +52,9 @@ constexpr int EPI_BYTES = 32 * 128;     // per epilogue warp: 32 rows x 64 bf16
 template <int EW> struct PairCfg {
   static constexpr int STAGES = EW == 4 ? 6 : 5;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * EPI_BYTES + 1024;
-  static constexpr int THREADS = 32 * (3 + EW);
+  static constexpr int THREADS = 32 * (4 + EW);
   static constexpr int RELAY = 2 + EW;   // warp index of the relay
+  static constexpr int MMA2 = 3 + EW;    // warp index of the second MMA issuer
 };
 constexpr uint32_t TMEM_COLS = 512;     // two accumulator buffers of 256 fp32 columns
 constexpr int SLAB = 64 * 128;          // one 64-element-wide, 64-row swizzled slab
@@ -226,7 +228,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
     tc_pair_dw_kernel(const __grid_constant__ PairParams p) {
   constexpr int STAGES = PairCfg<EW>::STAGES;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t land_bar[STAGES], full_bar[STAGES], empty_bar[STAGES];
+  // full_bar[w][s]: stage s holds a K block of a tile of MMA issuer w (one set per issuer,
+  // so that neither issuer ever waits on a phase of the other's K blocks)
+  __shared__ __align__(8) uint64_t land_bar[STAGES], full_bar[2][STAGES], empty_bar[STAGES];
   __shared__ __align__(8) uint64_t tfull_bar[2], tempty_bar[2], final_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
@@ -246,14 +250,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
     abort_flag = 0;
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&land_bar[s]), 1);
-      mbar_init(smem_u32(&full_bar[s]), 2);     // the relays of both CTAs
+      mbar_init(smem_u32(&full_bar[0][s]), 2);  // the relays of both CTAs
+      mbar_init(smem_u32(&full_bar[1][s]), 2);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull_bar[b]), 1);
       mbar_init(smem_u32(&tempty_bar[b]), 2 * EW);   // the epilogue warps of both CTAs
     }
-    mbar_init(smem_u32(&final_bar), 1);
+    mbar_init(smem_u32(&final_bar), 2);        // one commit from each MMA issuer
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -305,12 +310,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
         mbar_wait_bounded(smem_u32(&land_bar[s]), (pend_par >> s) & 1u, nullptr, a.err, kWaitLimitNs);
   } else if (warp == PairCfg<EW>::RELAY) {
     // ------------------------------------------------------------ relay (both CTAs)
-    int stage = 0;
+    int stage = 0, it = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (TileCursor cur(sched, ng, pair, npairs); cur.valid() && ok; cur.advance()) {
+    for (TileCursor cur(sched, ng, pair, npairs); cur.valid() && ok; cur.advance(), ++it) {
       const TileCoord tc = cur.coord(a, MODE, PM, s_off);
       const int nkb = (tc.G.K + BK - 1) / BK;
+      const int w = it & 1;   // the issuer of this tile
       for (int kb = 0; kb < nkb; ++kb) {
         const bool got = mbar_wait_bounded(smem_u32(&land_bar[stage]), phase, &abort_flag, a.err,
                                            kWaitLimitNs);
@@ -328,31 +334,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(peer_addr(smem_u32(&full_bar[stage]), 0));
+        if (lane == 0) mbar_arrive_remote(peer_addr(smem_u32(&full_bar[w][stage]), 0));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (even CTA)
+  } else if (warp == 1 || warp == PairCfg<EW>::MMA2) {
+    // ------------------------------------------------------------ MMA issuers (even CTA)
+    // Two threads in different warps issue alternate tiles, issuer w the tiles that use
+    // accumulator w, so that one thread's waits and bookkeeping between K blocks overlap
+    // the other's MMAs (a single issuing thread leaves the tensor pipe idle there). Each
+    // walks the whole tile sequence to keep its place in the stage ring; a commit covers
+    // only the committing thread's own MMAs, which are the ones that read its stages.
+    const int w = warp == 1 ? 0 : 1;
     if (leader && lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(PM, BN, true, true);
       int stage = 0;
-      uint32_t phase = 0;
-      bool issued = false, ok = true;
+      uint32_t fpar = 0;   // per stage: parity of this issuer's next wait on full_bar[w][stage]
+      bool ok = true;
       int it = 0;
       for (TileCursor cur(sched, ng, pair, npairs); cur.valid() && ok; cur.advance(), ++it) {
         const TileCoord tc = cur.coord(a, MODE, PM, s_off);
         const int nkb = (tc.G.K + BK - 1) / BK;
         const int b = it & 1;
+        if (b != w) {   // the other issuer's tile: step over its K blocks in the ring
+          stage = (stage + nkb) % STAGES;
+          continue;
+        }
         if (!mbar_wait_bounded(smem_u32(&tempty_bar[b]), ((it >> 1) & 1) ^ 1, &abort_flag, a.err,
                                kWaitLimitNs)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full_bar[stage]), phase, &abort_flag, a.err, kWaitLimitNs)) {
+          if (!mbar_wait_bounded(smem_u32(&full_bar[w][stage]), (fpar >> stage) & 1u, &abort_flag, a.err,
+                                 kWaitLimitNs)) {
             ok = false;
             break;
           }
+          fpar ^= 1u << stage;
           tc_fence_after();
           const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
           // K=16 steps in this block: 4, or fewer in a ragged last block
@@ -363,11 +381,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
             umma_pair(d_tmem, sdesc(a_s + kk * 2048, SLAB, 1024), sdesc(b_s + kk * 2048, SLAB, 1024), idesc,
                       (kb | kk) != 0 ? 1u : 0u);
           }
-          issued = true;
           // the tile's last stage is released by the epilogue once the accumulator is full:
           // a commit straight after another one stalls the tensor pipe
           if (kb + 1 < nkb) umma_commit_mc(smem_u32(&empty_bar[stage]), 0x3);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == STAGES) stage = 0;
         }
         if (!ok) break;
         if (nkb > 0) {
@@ -377,10 +394,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
           mbar_arrive_remote(peer_addr(smem_u32(&tfull_bar[b]), 1));
         }
       }
-      if (issued) {  // every MMA of the pair retired before the tensor memory is released
-        umma_commit_mc(smem_u32(&final_bar), 0x1);
-        mbar_wait_bounded(smem_u32(&final_bar), 0, nullptr, a.err, kWaitLimitNs);
-      }
+      // every MMA of both issuers retired before the tensor memory is released (a commit
+      // with no MMA before it arrives at once)
+      umma_commit_mc(smem_u32(&final_bar), 0x1);
+      mbar_wait_bounded(smem_u32(&final_bar), 0, nullptr, a.err, kWaitLimitNs);
     }
     __syncwarp();
   } else {
