@@ -46,6 +46,21 @@ __device__ __forceinline__ void tma_store3d(const CUtensorMap* map, uint32_t src
                "r"(src), "r"(c0), "r"(c1), "r"(c2)
                : "memory");
 }
+// The same store with an L2 cache policy (from l2_evict_first()): a result written once and
+// not read back should not push out of L2 the operands that later tiles re-read.
+__device__ __forceinline__ void tma_store3d_hint(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
