@@ -61,9 +61,13 @@ extern "C" int moe_permute_noalloc(const void* x, const int32_t* topk_idx, const
   if (dims == nullptr) return MOE_ERR_NULL_POINTER;
   if (dims->dtype != MOE_F32 && dims->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED_DTYPE;
   if (dims->k < 1 || dims->k > kMaxK || (dims->E >= 1 && dims->k > dims->E)) return MOE_ERR_BAD_TOPK;
-  if (dims->T < 0 || dims->E < 1 || dims->E > kMaxE || dims->d < 1 || dims->d % 8 != 0)
+  // the same row-width rule as moe_permute: d a multiple of 64 (bf16) or 8 (fp32)
+  const int unit = dims->dtype == MOE_BF16 ? 64 : 8;
+  if (dims->T < 0 || dims->E < 1 || dims->E > kMaxE || dims->d < 1 || dims->d % unit != 0)
     return MOE_ERR_BAD_DIMS;
   if (dims->capacity != 0) return MOE_ERR_BAD_DIMS;   // the dropless permutation only
+  // bound T before any product of it is formed (k >= 1, so T <= T*k)
+  if (dims->T > kNoAllocMaxCopies) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const int64_t copies = dims->T * dims->k;
   const int64_t n_chunks = (dims->T + kChunk - 1) / kChunk;
   if (copies > kNoAllocMaxCopies || dims->E * n_chunks > kNoAllocMaxChunkCells)
@@ -79,6 +83,8 @@ extern "C" int moe_permute_noalloc(const void* x, const int32_t* topk_idx, const
       (topk_w != nullptr && !aligned16(topk_w)))
     return MOE_ERR_MISALIGNED;
   if (w_perm != nullptr && topk_w == nullptr && !t0) return MOE_ERR_NULL_POINTER;
+  // the kernels update the error word with 32-bit atomics
+  if (dev_err != nullptr && (reinterpret_cast<uintptr_t>(dev_err) & 3u) != 0) return MOE_ERR_MISALIGNED;
   const cudaStream_t st = (cudaStream_t)stream;
   if (t0)
     return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (dims->E + 1), st) == cudaSuccess ? MOE_OK

@@ -142,12 +142,15 @@ int moe_permute(const void* x, const int32_t* topk_idx, const float* topk_w, con
 
 /* a2 without a workspace, for callers that cannot allocate device memory (an allocator-free
  * runtime, a memory pool that must not grow, a process limited to the buffers it was given).
- * The pages have no counterpart of this call. Same inputs, outputs and results as moe_permute;
- * the permutation's scratch lives in one static device array of the library (about 1.5 MB,
- * held by every GPU that loads the library until the process exits) instead of a workspace.
+ * The pages have no counterpart of this call. Same outputs and results as moe_permute for the
+ * dropless permutation (dims->capacity must be 0; f, S and f_s are not read), with the same
+ * row-width rule (d a multiple of 64 for bf16, of 8 for fp32); the permutation's scratch lives
+ * in one static device array of the library (about 1.5 MB, held by every GPU that loads the
+ * library until the process exits) instead of a workspace.
  * Limits: T*k <= 262144 and E * ceil(T/64) <= 65536, else MOE_ERR_WORKSPACE_TOO_SMALL (nothing
- * launched). dev_err: optional device int that receives MOE_ERR_DEVICE_EXPERT_ID for invalid
- * ids (first error wins; the caller zeroes it), or NULL. The first call on a device looks up the
+ * launched). dev_err: optional 4-byte-aligned device int (else MOE_ERR_MISALIGNED) that
+ * receives MOE_ERR_DEVICE_EXPERT_ID for invalid ids (first error wins; the caller zeroes it),
+ * or NULL. The first call on a device looks up the
  * array's address for that device; make it before any stream capture. Every call shares the
  * array: calls that overlap on the GPU race, so order them on one stream. */
 int moe_permute_noalloc(const void* x, const int32_t* topk_idx, const float* topk_w,

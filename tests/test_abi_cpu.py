@@ -115,3 +115,23 @@ def test_import_fails_loudly_without_library(tmp_path, monkeypatch):
         monkeypatch.undo()
         sys.modules.pop("dropless_token_routing_gb300._native", None)
         importlib.import_module("dropless_token_routing_gb300._native")
+
+
+def test_noalloc_permute_rejects_bad_calls_before_launching():
+    """The workspace-free permutation checks sizes, widths and pointers on the host; every call
+    here is rejected before any CUDA API is touched (the fake addresses are never used)."""
+    def bf16(**kw):
+        return dims(dtype=N.MOE_BF16, f=64, **kw)
+
+    def call(dm, x_perm=GOOD, dest=GOOD, dev_err=None):
+        return L.moe_permute_noalloc(GOOD, GOOD, GOOD, ctypes.byref(dm), x_perm, dest, GOOD, GOOD,
+                                     GOOD, dev_err, None)
+
+    assert call(bf16(T=40000, d=64, E=16, k=8)) == _code("MOE_ERR_WORKSPACE_TOO_SMALL")   # T*k > 2^18
+    assert call(bf16(T=8192, d=64, E=1024, k=2)) == _code("MOE_ERR_WORKSPACE_TOO_SMALL")  # E*T/64 > 2^16
+    assert call(bf16(T=2 ** 62, d=64, E=16, k=8)) == _code("MOE_ERR_WORKSPACE_TOO_SMALL")  # T*k overflows
+    assert call(bf16(T=256, d=72, E=16, k=2)) == _code("MOE_ERR_BAD_DIMS")                 # bf16: d % 64
+    ok = bf16(T=256, d=128, E=16, k=2)
+    assert call(ok, dev_err=GOOD + 2) == _code("MOE_ERR_MISALIGNED")   # not a 32-bit atomic's word
+    assert call(ok, x_perm=BAD) == _code("MOE_ERR_MISALIGNED")
+    assert call(ok, dest=None) == _code("MOE_ERR_NULL_POINTER")

@@ -60,16 +60,58 @@ def test_noalloc_permute_matches_workspace_permute_twice(T, E, k, d, dtype):
     assert np.array_equal(ref["dest"].cpu().numpy(), O.permutation(idx, E)[0])
 
 
-def test_noalloc_permute_rejects_problems_beyond_its_scratch():
+def _noalloc(lib, x, topk_idx, topk_w, dims, out, err):
+    stream = torch.cuda.current_stream().cuda_stream
+    return lib.moe_permute_noalloc(_p(x), _p(topk_idx), _p(topk_w), ctypes.byref(dims),
+                                   _p(out["x_perm"]), _p(out["dest"]), _p(out["row_src"]),
+                                   _p(out["offsets"]), _p(out["w_perm"]), _p(err), stream)
+
+
+def test_noalloc_permute_reports_invalid_ids_like_the_workspace_permute():
+    """An id outside [0, E) and an id repeated within a row are reported in the caller's error
+    word; those copies get dest = -1 and move no row, exactly as in moe_permute."""
+    from dropless_token_routing_gb300 import _native as N
+    from dropless_token_routing_gb300.api import Workspace, get_device_error, make_dims, permute
+    lib = N.lib()
+    T, E, k, d = 300, 16, 4, 128
+    g = torch.Generator().manual_seed(11)
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    idx[5, 2] = E            # out of range
+    idx[17, 0] = -1          # out of range
+    idx[40, 3] = idx[40, 1]  # repeated within the row
+    gate = torch.rand(T, k, generator=g, dtype=torch.float32)
+    x = torch.randn(T, d, generator=g).to(torch.bfloat16).cuda()
+    topk_idx, topk_w = idx.cuda(), gate.cuda()
+    dims = make_dims(T, d, E, k, 64, dtype=torch.bfloat16)
+    ref = _outputs(T, d, E, k, torch.bfloat16)
+    ws = Workspace(dims)
+    permute(x, topk_idx, topk_w, dims, ref["x_perm"], ref["dest"], ref["row_src"], ref["offsets"],
+            ref["w_perm"], ws)
+    assert get_device_error(ws) == N.STATUS_CODE["MOE_ERR_DEVICE_EXPERT_ID"]
+    dest = ref["dest"].cpu().view(T, k)
+    assert dest[5, 2] == -1 and dest[17, 0] == -1 and dest[40, 3] == -1 and dest[40, 1] >= 0
+    for call in range(2):
+        out = _outputs(T, d, E, k, torch.bfloat16)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        st = _noalloc(lib, x, topk_idx, topk_w, dims, out, err)
+        assert st == 0, N.status_string(st)
+        torch.cuda.synchronize()
+        assert err.item() == N.STATUS_CODE["MOE_ERR_DEVICE_EXPERT_ID"], call
+        for name in ("dest", "row_src", "offsets", "x_perm", "w_perm"):
+            assert torch.equal(out[name], ref[name]), (call, name)
+
+
+def test_noalloc_permute_with_no_tokens_writes_zero_offsets():
     from dropless_token_routing_gb300 import _native as N
     from dropless_token_routing_gb300.api import make_dims
     lib = N.lib()
-    fake = 0x10000  # never dereferenced: the size check comes first
-    too_many_copies = make_dims(40000, 64, 16, 8, 64, dtype=torch.bfloat16)   # T*k > 262144
-    st = lib.moe_permute_noalloc(fake, fake, fake, ctypes.byref(too_many_copies), fake, fake, fake,
-                                 fake, fake, None, None)
-    assert st == N.STATUS_CODE["MOE_ERR_WORKSPACE_TOO_SMALL"]
-    too_many_cells = make_dims(8192, 64, 1024, 2, 64, dtype=torch.bfloat16)   # E*T/64 > 65536
-    st = lib.moe_permute_noalloc(fake, fake, fake, ctypes.byref(too_many_cells), fake, fake, fake,
-                                 fake, fake, None, None)
-    assert st == N.STATUS_CODE["MOE_ERR_WORKSPACE_TOO_SMALL"]
+    E = 32
+    dims = make_dims(0, 256, E, 4, 64, dtype=torch.bfloat16)
+    offsets = torch.full((E + 1,), -7, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    st = lib.moe_permute_noalloc(None, None, None, ctypes.byref(dims), None, None, None,
+                                 _p(offsets), None, _p(err), stream)
+    assert st == 0, N.status_string(st)
+    torch.cuda.synchronize()
+    assert not offsets.any() and err.item() == 0
