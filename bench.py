@@ -208,31 +208,41 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- oracle arm
-def oracle_sample(w, logits32, n_tokens, with_w_r=True):
-    """Time the fp64 oracle's forward + backward on the first n_tokens tokens of a workload
-    (its routing taken from the device's fp32 scores; only the experts those tokens use)."""
+def oracle_scale(cfg):
+    """Scale-down factor of the oracle's sample: T / s tokens routed among E / s experts (every
+    s-th expert), so that every expert keeps the workload's mean segment of T*k/E copies and
+    every token the workload's work (k routed copies at the full d and f, plus the shared
+    experts). s is the largest power of two up to 16 that leaves at least 2k experts."""
+    s = 16
+    while s > 1 and cfg["E"] // s < 2 * cfg["k"]:
+        s //= 2
+    return s
+
+
+def oracle_sample(w, logits32, scale):
+    """Time the fp64 oracle's forward + backward (layer_forward + layer_backward, as they stand)
+    on a sub-layer of the workload: its first T/scale tokens routed (top-k, renormalised) among
+    every scale-th expert, with the full d, f and shared experts. The routing is taken from the
+    device's fp32 scores restricted to those experts. Returns (seconds, tokens, experts)."""
     import numpy as np
+    import torch
     import oracle as O
     c = w.cfg
-    rows = slice(0, n_tokens)
-    bias = None if w.bias is None else w.bias.cpu().numpy()
-    idx, gate = O.route_topk(O.selection_scores(logits32[rows], bias), c["k"])
-    used = np.unique(idx)
-    remap = {int(e): i for i, e in enumerate(used)}
-    idx_s = np.vectorize(remap.get)(idx)
-    x = O.as_f64(w.x[rows].cpu())
-    dy = O.as_f64(w.dy[rows].cpu())
-    sel = __import__("torch").as_tensor(used)
-    w13 = O.as_f64(w.w13[sel.to(w.w13.device)].cpu())
-    w2 = O.as_f64(w.w2[sel.to(w.w2.device)].cpu())
-    ws13 = None if w.ws13 is None else O.as_f64(w.ws13.cpu())
-    ws2 = None if w.ws2 is None else O.as_f64(w.ws2.cpu())
-    w_r = O.as_f64(w.w_r[:, sel.to(w.w_r.device)].cpu()) if (with_w_r and w.w_r is not None) else None
+    Ts, cols = c["T"] // scale, np.arange(0, c["E"], scale)
+    bias = None if w.bias is None else w.bias.cpu().numpy()[cols]
+    idx, gate = O.route_topk(O.selection_scores(np.ascontiguousarray(logits32[:Ts][:, cols]), bias), c["k"])
+    sel = torch.as_tensor(cols).to(w.w13.device)
+
+    def f64(t):     # exact upcast on the tensor's own device, then to host memory
+        return None if t is None else t.double().cpu().numpy()
+    x, dy = f64(w.x[:Ts]), f64(w.dy[:Ts])
+    w13, w2 = f64(w.w13[sel]), f64(w.w2[sel])
+    ws13, ws2 = f64(w.ws13), f64(w.ws2)
+    w_r = None if w.w_r is None else f64(w.w_r[:, sel])
     t0 = time.perf_counter()
-    fwd = O.layer_forward(x, idx_s, gate, w13, w2, ws13, ws2)
-    O.layer_backward(x, idx_s, gate, fwd, dy, w13, w2, ws13, ws2, w_r=w_r)
-    dt = time.perf_counter() - t0
-    return dt, len(used)
+    fwd = O.layer_forward(x, idx, gate, w13, w2, ws13, ws2)
+    O.layer_backward(x, idx, gate, fwd, dy, w13, w2, ws13, ws2, w_r=w_r)
+    return time.perf_counter() - t0, Ts, len(cols)
 
 
 def blas_threads():
@@ -246,11 +256,23 @@ def blas_threads():
     return os.cpu_count()
 
 
-def cpu_baseline(w, logits32, n_tokens):
-    dt, n_exp = oracle_sample(w, logits32, n_tokens)
-    return {"value": n_tokens / dt, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": f"fp64 oracle fwd+bwd of the first {n_tokens} tokens of the workload "
-                      f"({n_exp} routed experts they use + shared, full d/f), {dt:.1f} s"}
+def sample_text(cfg, scale, Ts, Es):
+    return (f"fp64 oracle (layer_forward + layer_backward) on a 1/{scale} sub-layer of the workload: "
+            f"its first {Ts} tokens routed top-{cfg['k']} among {Es} of its {cfg['E']} experts "
+            f"(every {scale}th), {Ts * cfg['k'] // Es} copies per expert on average as in the full "
+            f"layer, full d={cfg['d']}, f={cfg['f']} and {cfg['S']} shared expert(s); the per-token "
+            f"work equals the full layer's, so tokens/s is the oracle's rate on this workload")
+
+
+def cpu_baseline(w, logits32, min_seconds=10.0):
+    """The oracle's tokens/s: the sub-layer sample repeated until about min_seconds of CPU work."""
+    scale = oracle_scale(w.cfg)
+    tot, toks, runs = 0.0, 0, 0
+    while tot < min_seconds or runs == 0:
+        dt, Ts, Es = oracle_sample(w, logits32, scale)
+        tot, toks, runs = tot + dt, toks + Ts, runs + 1
+    return {"value": toks / tot, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": sample_text(w.cfg, scale, Ts, Es) + f"; {runs} run(s), {tot:.1f} s"}
 
 
 # --------------------------------------------------------------------------- layer variants
@@ -310,6 +332,128 @@ def fused_rearrange(params, cfg, w, args, stream):
     return {"value": round(cfg["T"] / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3)}
 
 
+# --------------------------------------------------------------------------- summaries
+def summarize(cfg, trace, steps, counts, peaks):
+    """Per-kernel table, grouped-GEMM totals and routing statistics of a traced run of
+    `steps` layer steps (trace: phase -> (launches, total ms))."""
+    flops, bytes_ = algorithmic_work(cfg)
+    total_ms = sum(v[1] for v in trace.values())
+    kernels = {}
+    for name, (launches, ms) in sorted(trace.items(), key=lambda kv: -kv[1][1]):
+        # every phase is one operation per step, possibly of several launches (the dW_r
+        # partial sums and their reduction; the router's weight split and its GEMM), so
+        # the operation's work is divided by the phase's time per step
+        per = ms / launches
+        per_step = ms / steps
+        ent = {"launches_per_step": launches / steps, "ms_per_launch": round(per, 4),
+               "ms_per_step": round(per_step, 4),
+               "share": round(ms / total_ms, 4) if total_ms else None}
+        if name in flops and name != "router_gemm":
+            ach = flops[name] / (per_step / 1e3) / 1e12
+            ent.update(achieved=round(ach, 1), unit="TFLOP/s",
+                       frac=round(ach / peaks["bf16_tflops_sustained"], 3))
+        elif name in bytes_:
+            ach = bytes_[name] / (per_step / 1e3) / 1e9
+            ent.update(achieved=round(ach, 1), unit="GB/s", frac=round(ach / peaks["hbm_gbs"], 3))
+        elif name == "router_gemm":
+            if cfg["dtype"] == "f32":
+                ent.update(achieved=round(flops[name] / (per_step / 1e3) / 1e12, 2),
+                           unit="TFLOP/s (fp32 FMA)")
+            else:   # three bf16 parts of the fp32 weight, each a full product on the tensor cores
+                ent.update(achieved=round(3 * flops[name] / (per_step / 1e3) / 1e12, 1),
+                           unit="TFLOP/s (bf16, 3-part weight split, executed)")
+        kernels[name] = ent
+    groof = group_roofline(cfg, counts, peaks)
+    for name, g in groof.items():
+        if name in kernels:
+            ms = kernels[name]["ms_per_step"]
+            kernels[name]["group_roofline"] = {
+                "per_group_ms": round(g["per_group_ms"], 4), "frac": round(g["per_group_ms"] / ms, 3),
+                "whole_launch_ms": round(g["whole_launch_ms"], 4),
+                "frac_whole_launch": round(g["whole_launch_ms"] / ms, 3)}
+    # the dominant kernel: the phase with the most time among those with algorithmic work
+    # (the router GEMM aside, whose executed FLOPs are three times its algorithmic ones)
+    ranked = [kv for kv in trace.items() if (kv[0] in flops and kv[0] != "router_gemm") or kv[0] in bytes_]
+    dom = max(ranked or trace.items(), key=lambda kv: kv[1][1])[0]
+    gemm_names = [k_ for k_ in trace if k_.startswith("gemm")]
+    gemm_flops = sum(flops[k_] for k_ in gemm_names)
+    gemm_ms = sum(trace[k_][1] for k_ in gemm_names) / steps
+    groof_ms = sum(g["per_group_ms"] for n_, g in groof.items() if n_ in trace)
+    tf = gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms else 0.0
+    T = cfg["T"]
+    rows = sum(counts) + cfg["S"] * T
+    padded = sum(-(-c // 128) * 128 for c in counts) + cfg["S"] * (-(-T // 128) * 128)
+    return {
+        "kernels": kernels, "dominant": dom, "launches": sum(v[0] for v in trace.values()),
+        "grouped_gemm": {"tflops": round(tf, 1),
+                         "frac_of_dense_peak": round(tf / peaks["bf16_tflops_sustained"], 3),
+                         "frac_of_burst_peak": round(tf / peaks["bf16_tflops"], 3),
+                         "peak_kind": f"useful FLOPs; dense bf16 sustained / burst ({peaks['source']})",
+                         "per_group_roofline_ms": round(groof_ms, 3),
+                         "frac_of_per_group_roofline": round(groof_ms / gemm_ms, 3) if gemm_ms else None},
+        "routing": {"max_expert_rows": max(counts), "empty_experts": sum(1 for c in counts if c == 0),
+                    "m_tile_fill": round(rows / padded, 4)}}
+
+
+def other_workload(name, args, dev, peaks, steps=10):
+    """Time another workload the same way as the main one (fwd + bwd on device-resident
+    inputs, `steps` steps after the warm-up, per-kernel CUDA-event trace). A workload whose
+    recipe is forward-only (the mid-size one) is also timed forward-only."""
+    import torch
+    from dropless_token_routing_gb300 import _native as N
+    from dropless_token_routing_gb300.api import LayerParams, MoELayer, get_device_error
+    from synth import CONFIGS, make_workload
+    cfg = dict(CONFIGS[name], name=name)
+    T = cfg["T"]
+    w = make_workload(cfg, device=dev)
+    params = LayerParams(w13=w.w13, w2=w.w2, w_r=w.w_r, bias=w.bias, ws13=w.ws13, ws2=w.ws2)
+    layer = MoELayer(params, T, cfg["d"], cfg["E"], cfg["k"], cfg["f"], cfg["S"], cfg["f_s"],
+                     w.torch_dtype, device=dev, logits_input=w.logits_in is not None)
+    layer.alloc_grads()
+    stream = torch.cuda.current_stream()
+
+    def run(n, bwd=True):
+        for _ in range(n):
+            layer.forward(w.x, w.logits_in)
+            if bwd:
+                layer.backward(w.dy)
+
+    run(args.warmup)
+    torch.cuda.synchronize()
+    N.trace_enable(True)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    run(steps)
+    b.record(stream)
+    torch.cuda.synchronize()
+    trace = N.trace_read()
+    N.trace_enable(False)
+    ms = a.elapsed_time(b) / steps
+    out = {"workload": f"T={T} d={cfg['d']} E={cfg['E']} top-{cfg['k']} f={cfg['f']} S={cfg['S']} "
+                       f"f_s={cfg['f_s']} routing={cfg['routing']}"
+                       + (f"(s={cfg['zipf_s']})" if cfg["routing"] == "zipf" else ""),
+           "steps": steps, "ms_per_step": round(ms, 3), "value": round(T / (ms / 1e3), 1), "unit": UNIT}
+    if not cfg["bwd"]:     # the recipe itself is forward-only
+        c, d_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c.record(stream)
+        run(steps, bwd=False)
+        d_.record(stream)
+        torch.cuda.synchronize()
+        fms = c.elapsed_time(d_) / steps
+        out["forward_only"] = {"ms_per_step": round(fms, 3), "value": round(T / (fms / 1e3), 1),
+                               "unit": "tokens/s forward"}
+    if get_device_error(layer.ws) != 0:
+        raise RuntimeError(f"device error in the {name} run")
+    summ = summarize(cfg, trace, steps, layer.saved["counts"].cpu().tolist(), peaks)
+    out.update(grouped_gemm=summ["grouped_gemm"], routing=summ["routing"])
+    keep = ("permute_scatter", "permute_rows", "combine", "combine_bwd")
+    out["hbm_frac"] = {k_: summ["kernels"][k_]["frac"] for k_ in keep if k_ in summ["kernels"]}
+    out["gemm_frac"] = {k_: summ["kernels"][k_]["frac"] for k_ in summ["kernels"] if k_.startswith("gemm")}
+    del layer, params, w
+    torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -319,12 +463,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="pangu_bf16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--oracle-tokens", type=int, default=4)
     ap.add_argument("--shrink", default="", help="smaller case of the same recipe, e.g. T=512,E=16 "
                                                   "(for profiler captures; not a bench line)")
     ap.add_argument("--no-fused-rearrange", dest="fused_rearrange", action="store_false",
                     help="skip the timing of the fused-rearrangement variant (rank 0, after the "
                          "main measurement)")
+    ap.add_argument("--other-workloads", default="dsv3_bf16,adversarial_bf16,mid_bf16",
+                    help="further workloads timed after the main one (rank 0, 10 steps each; empty "
+                         "to skip); each gets its own entry in the line's other_workloads")
     ap.add_argument("--drop-pad", default="1.0,1.25",
                     help="capacity factors of the drop-and-pad comparison runs (rank 0, after the "
                          "dropless measurement; empty to skip)")
@@ -362,25 +508,26 @@ def main():
         w = make_workload(cfg, device=dev)
         if w.logits_in is not None:
             logits32 = w.logits_in.cpu().numpy()
-        else:
+        else:       # fp32 scores of the sampled tokens (the oracle's own router, rounded to fp32)
             import oracle as O
-            logits32 = O.router_logits(O.as_f64(w.x[:args.oracle_tokens].cpu()),
-                                       O.as_f64(w.w_r.cpu())).astype("float32")
-        for _ in range(args.warmup if False else 0):
-            pass
+            scale = oracle_scale(cfg)
+            logits32 = O.router_logits(w.x[:T // scale].double().cpu().numpy(),
+                                       w.w_r.double().cpu().numpy()).astype("float32")
+        scale = oracle_scale(cfg)
+        for _ in range(args.warmup):
+            oracle_sample(w, logits32, scale)
         times = []
         for _ in range(args.steps):
-            dt, n_exp = oracle_sample(w, logits32, args.oracle_tokens)
+            dt, Ts, Es = oracle_sample(w, logits32, scale)
             times.append(dt)
         tot = sum(times)
-        value = args.steps * args.oracle_tokens / tot
+        value = args.steps * Ts / tot
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": workload_cfg,
                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                                 "sample": f"each step: fp64 oracle fwd+bwd of the first {args.oracle_tokens} "
-                                           f"tokens ({n_exp} routed experts + shared, full d/f)"},
+                                 "sample": "each step: " + sample_text(cfg, scale, Ts, Es)},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -513,39 +660,13 @@ def main():
 
     # ---------------------------------------------------------------- roofline
     peaks = _peaks()
-    flops, bytes_ = algorithmic_work(cfg)
-    total_ms = sum(v[1] for v in trace.values())
-    kernels = {}
-    for name, (launches, ms) in sorted(trace.items(), key=lambda kv: -kv[1][1]):
-        # every phase is one operation per step, possibly of several launches (the dW_r
-        # partial sums and their reduction; the router's weight split and its GEMM), so
-        # the operation's work is divided by the phase's time per step
-        per = ms / launches
-        per_step = ms / args.steps
-        ent = {"launches_per_step": launches / args.steps, "ms_per_launch": round(per, 4),
-               "ms_per_step": round(per_step, 4),
-               "share": round(ms / total_ms, 4) if total_ms else None}
-        if name in flops and name != "router_gemm":
-            ach = flops[name] / (per_step / 1e3) / 1e12
-            ent.update(achieved=round(ach, 1), unit="TFLOP/s",
-                       frac=round(ach / peaks["bf16_tflops_sustained"], 3))
-        elif name in bytes_:
-            ach = bytes_[name] / (per_step / 1e3) / 1e9
-            ent.update(achieved=round(ach, 1), unit="GB/s", frac=round(ach / peaks["hbm_gbs"], 3))
-        elif name == "router_gemm":
-            if cfg["dtype"] == "f32":
-                ent.update(achieved=round(flops[name] / (per_step / 1e3) / 1e12, 2),
-                           unit="TFLOP/s (fp32 FMA)")
-            else:   # three bf16 parts of the fp32 weight, each a full product on the tensor cores
-                ent.update(achieved=round(3 * flops[name] / (per_step / 1e3) / 1e12, 1),
-                           unit="TFLOP/s (bf16, 3-part weight split, executed)")
-        kernels[name] = ent
-    # the dominant kernel: the phase with the most time among those with algorithmic work
-    # (the router GEMM aside, whose executed FLOPs are three times its algorithmic ones)
-    ranked = [kv for kv in trace.items() if (kv[0] in flops and kv[0] != "router_gemm") or kv[0] in bytes_]
-    dom = max(ranked or trace.items(), key=lambda kv: kv[1][1])[0]
+    cnt = layer.saved["counts"].cpu().tolist()
+    summ = summarize(cfg, trace, args.steps, cnt, peaks)
+    kernels, launches = summ["kernels"], summ["launches"]
+    dom = summ["dominant"]
     dl, dms = trace[dom]
     per = dms / dl
+    flops, bytes_ = algorithmic_work(cfg)
     traffic = None
     tr = NCU_TRAFFIC.get(dom)
     # the captured bytes hold only for the workload they were captured on
@@ -558,7 +679,8 @@ def main():
         peak = peaks["bf16_tflops_sustained"]
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(ach / peak, 3), "traffic": traffic, "kernel": dom,
-                "peak_kind": f"bf16 dense, sustained ({peaks['source']})"}
+                "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
+                "frac_of_burst_peak": round(ach / peaks["bf16_tflops"], 3)}
     else:
         ach = bytes_[dom] / (per / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -573,43 +695,25 @@ def main():
         roof["write_stream"] = {"bytes": wb, "achieved": round(wach, 1), "peak": peaks["hbm_gbs"],
                                 "unit": "GB/s", "frac": round(wach / peaks["hbm_gbs"], 3),
                                 "peak_kind": f"HBM copy ({peaks['source']})"}
-    gemm_flops = sum(v for k_, v in flops.items() if k_.startswith("gemm"))
-    gemm_ms = sum(trace[k_][1] for k_ in trace if k_.startswith("gemm")) / args.steps
-    launches = sum(v[0] for v in trace.values())
-
-    cnt = layer.saved["counts"].cpu().tolist()
-    groof = group_roofline(cfg, cnt, peaks)
-    for name, g in groof.items():
-        if name in kernels:
-            ms = kernels[name]["ms_per_step"]
-            kernels[name]["group_roofline"] = {
-                "per_group_ms": round(g["per_group_ms"], 4), "frac": round(g["per_group_ms"] / ms, 3),
-                "whole_launch_ms": round(g["whole_launch_ms"], 4),
-                "frac_whole_launch": round(g["whole_launch_ms"] / ms, 3)}
-    groof_ms = sum(g["per_group_ms"] for n_, g in groof.items() if n_ in trace)
-    rows = sum(cnt) + cfg["S"] * T
-    padded = sum(-(-c // 128) * 128 for c in cnt) + cfg["S"] * (-(-T // 128) * 128)
-    routing_stats = {"max_expert_rows": max(cnt), "empty_experts": sum(1 for c in cnt if c == 0),
-                     "m_tile_fill": round(rows / padded, 4)}
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_ms / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype_name,
             "data": "synthetic (seeded, device-generated)", "config": workload_cfg,
             "roofline": roof, "gpu_launches": launches, "e2e": e2e, "clocks": clocks,
-            "grouped_gemm": {"tflops": round(gemm_flops / (gemm_ms / 1e3) / 1e12, 1),
-                             "frac_of_dense_peak": round(gemm_flops / (gemm_ms / 1e3) / 1e12 /
-                                                         peaks["bf16_tflops_sustained"], 3),
-                             "per_group_roofline_ms": round(groof_ms, 3),
-                             "frac_of_per_group_roofline": round(groof_ms / gemm_ms, 3) if gemm_ms else None},
-            "routing": routing_stats, "kernels": kernels}
+            "grouped_gemm": summ["grouped_gemm"], "routing": summ["routing"], "kernels": kernels}
     if not args.no_cpu_baseline and world == 1:
         logits32 = (li if li is not None else layer.saved["logits"]).cpu().numpy()
-        line["cpu_baseline"] = cpu_baseline(w, logits32, args.oracle_tokens)
+        line["cpu_baseline"] = cpu_baseline(w, logits32)
     factors = [float(v) for v in args.drop_pad.split(",") if v.strip()]
     if factors:
         line["drop_and_pad"] = drop_and_pad(factors, params, cfg, w, cnt, args, stream)
     if args.fused_rearrange and cfg["dtype"] == "bf16":
         line["fused_rearrange"] = fused_rearrange(params, cfg, w, args, stream)
+    others = [n for n in args.other_workloads.split(",") if n.strip() and n.strip() != args.config]
+    if others and not args.shrink:
+        del layer, params, w, x, dy, li, d_in, h_x, h_dy, h_li, h_y, h_dx
+        torch.cuda.empty_cache()
+        line["other_workloads"] = {n: other_workload(n.strip(), args, dev, peaks) for n in others}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

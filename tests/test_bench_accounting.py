@@ -65,3 +65,39 @@ def test_dw_write_bytes():
     w = bench.dw_write_bytes(CFG)
     assert w["gemm_dw13"] == 2 * (2 * 64 * 128 * 2 + 2 * 64 * 128 * 1)
     assert w["gemm_dw2"] == w["gemm_dw13"] // 2
+
+
+def test_oracle_scale_keeps_twice_k_experts():
+    assert bench.oracle_scale({"E": 256, "k": 8}) == 16       # 16 experts, 256 copies each
+    assert bench.oracle_scale({"E": 64, "k": 6}) == 4         # 16 >= 12 experts
+    assert bench.oracle_scale({"E": 8, "k": 2}) == 2
+    assert bench.oracle_scale({"E": 2, "k": 2}) == 1
+
+
+def test_oracle_sample_runs_a_sub_layer_on_cpu():
+    import numpy as np
+    import oracle as O
+    from synth import make_workload, shrink
+    w = make_workload(shrink("pangu_bf16", T=64, d=64, E=32, k=4, f=64, f_s=64))
+    s = bench.oracle_scale(w.cfg)
+    assert s == 4
+    logits32 = O.router_logits(O.as_f64(w.x), O.as_f64(w.w_r)).astype(np.float32)
+    dt, Ts, Es = bench.oracle_sample(w, logits32, s)
+    assert (Ts, Es) == (16, 8) and dt > 0
+    text = bench.sample_text(w.cfg, s, Ts, Es)
+    assert "16 tokens" in text and "8 of its 32 experts" in text and "8 copies per expert" in text
+
+
+def test_summarize_grouped_totals_and_dominant():
+    steps = 2
+    trace = {"gemm_fwd1": (2, 8.0), "gemm_dw13": (2, 10.0), "combine": (2, 1.0)}
+    counts = [100, 28]
+    r = bench.summarize(CFG, trace, steps, counts, PEAKS)
+    flops, bytes_ = bench.algorithmic_work(CFG)
+    assert r["dominant"] == "gemm_dw13" and r["launches"] == 6
+    tf = (flops["gemm_fwd1"] + flops["gemm_dw13"]) / (9.0 / 1e3) / 1e12
+    assert r["grouped_gemm"]["tflops"] == pytest.approx(tf, abs=0.06)
+    assert r["grouped_gemm"]["frac_of_burst_peak"] == pytest.approx(tf / 100.0, abs=1e-3)
+    assert r["kernels"]["combine"]["unit"] == "GB/s"
+    # 128-row M tiles: (100 + 28 + 64 rows) in 128 + 128 + 128 slots
+    assert r["routing"]["m_tile_fill"] == pytest.approx(192 / 384, abs=1e-4)
