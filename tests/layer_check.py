@@ -4,7 +4,8 @@ fp64 oracle on the same seeded inputs, and compare.
 Bars: bit-exact for routing indices, counts, offsets, dest, row_src and the permuted
 rows; ||gpu - oracle|| / ||oracle|| <= 1e-5 for fp32 workloads and for the fp32 gates
 and scores of every workload; <= 5e-3 for bf16 outputs and gradients, the score
-gradients (dlogits, dW_r) included.
+gradients (dlogits, dW_r) included, except those of bf16 layers with fewer than 16 tokens
+(<= 1e-2, see FEW_TOKENS below).
 
 MOE_PARITY_LOG=<file> appends one JSON line per checked case with every measured error."""
 from __future__ import annotations
@@ -19,6 +20,14 @@ import oracle as O
 
 TOL = {"f32": 1e-5, "bf16": 5e-3}
 GATE_TOL = 1e-5
+# Score gradients (dlogits, dW_r) of a bf16 layer with fewer than FEW_TOKENS tokens. The
+# gradient with respect to a gate, sum_f D * silu(a) * b, is formed from the bf16-rounded
+# pre-activations a and b that the forward stores; over many tokens the rounding errors
+# average to about 2.5e-3 of the score gradient, but for one token the error is a single
+# draw and reaches 5-8e-3 (rounding the exact pre-activations to bf16 on the host gives the
+# same error to three digits). Those tensors are held to this bar; every other case to TOL.
+FEW_TOKENS = 16
+FEW_TOKENS_SCORE_TOL = 1e-2
 
 
 def rel(gpu, ref) -> float:
@@ -124,9 +133,11 @@ def check_layer(w, bwd=True, report=None, capacity=0, rearrange=0):
         errs["score_grad_cancellation"] = float(
             np.linalg.norm(ref["gate"] * b["dgate"]) / max(np.linalg.norm(b["dscores"]), 1e-300))
         _log(w, capacity, rearrange, errs)
+        few = w.cfg["dtype"] == "bf16" and w.cfg["T"] < FEW_TOKENS
         for n in ("dx", "dw13", "dw2", "dws13", "dws2", "dw_r", "dlogits"):
             if n in errs:
-                assert errs[n] <= tol, (n, errs)
+                bar = FEW_TOKENS_SCORE_TOL if (few and n in ("dw_r", "dlogits")) else tol
+                assert errs[n] <= bar, (n, errs)
         # experts without tokens keep exactly zero gradients
         empty = np.nonzero(fwd["counts"] == 0)[0]
         for e in empty:
