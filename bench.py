@@ -465,6 +465,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shrink", default="", help="smaller case of the same recipe, e.g. T=512,E=16 "
                                                   "(for profiler captures; not a bench line)")
+    ap.add_argument("--rearrange", default="copy", choices=["copy", "gather"],
+                    help="the timed step's rearrangement: rearranged copies (default) or TMA row "
+                         "gathers fused into the expert GEMMs (with selective recompute)")
     ap.add_argument("--no-fused-rearrange", dest="fused_rearrange", action="store_false",
                     help="skip the timing of the fused-rearrangement variant (rank 0, after the "
                          "main measurement)")
@@ -538,10 +541,14 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     w = make_workload(cfg, device=dev)
     params = LayerParams(w13=w.w13, w2=w.w2, w_r=w.w_r, bias=w.bias, ws13=w.ws13, ws2=w.ws2)
+    gather = args.rearrange == "gather"
     layer = MoELayer(params, T, cfg["d"], cfg["E"], cfg["k"], cfg["f"], cfg["S"], cfg["f_s"],
-                     w.torch_dtype, device=dev, logits_input=w.logits_in is not None)
+                     w.torch_dtype, device=dev, logits_input=w.logits_in is not None,
+                     rearrange=1 if gather else 0, recompute=gather)
     layer.alloc_grads()
     x, dy, li = w.x, w.dy, w.logits_in
+    if gather:
+        workload_cfg["rearrange"] = "TMA row gathers fused into the expert GEMMs"
     stream = torch.cuda.current_stream()
 
     def step():

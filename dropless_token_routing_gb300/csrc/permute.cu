@@ -214,8 +214,10 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const T* __restrict__
 
 // ---------------------------------------------------------------- a4: combine
 // y[t] = sum_j w_j y_perm[dest_j] (+ y_sh[t]) (+ sum_j dl_j W_r^T[e_j]) in fp32, in that
-// order, rounded once. One warp per token, 8 elements per lane per step.
-template <typename T, bool ROUTER>
+// order, rounded once. One warp per token, 8 elements per lane per step. With k <= KMAX the
+// k rows' vectors of a step (and the shared expert's) are all requested before the sums
+// start, so a warp keeps k + 1 loads in flight instead of one; the sums keep their order.
+template <typename T, bool ROUTER, int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(
     const T* __restrict__ y_perm, const int32_t* __restrict__ dest, const float* __restrict__ topk_w,
     const T* __restrict__ y_sh, const int32_t* __restrict__ idx, const float* __restrict__ dl_tok,
@@ -234,6 +236,44 @@ __global__ void __launch_bounds__(256) combine_kernel(
         gq = dl_tok[q];
       }
     }
+    if constexpr (KMAX > 0) {
+      // every lane holds every copy's row and weight (uniform across the warp)
+      int dj[KMAX > 0 ? KMAX : 1];
+      float wj[KMAX > 0 ? KMAX : 1];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        dj[j] = __shfl_sync(0xffffffffu, dq, j);
+        wj[j] = __shfl_sync(0xffffffffu, wq, j);
+      }
+      for (int vb = 0; vb < nvec; vb += 32) {
+        const int v = vb + lane;
+        if (v >= nvec) break;        // no shuffles below: lanes may leave
+        Vec8<T> val[KMAX > 0 ? KMAX : 1], sh;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if (j < k && dj[j] >= 0) val[j].load(y_perm + (int64_t)dj[j] * d + (int64_t)v * 8);
+        if (y_sh != nullptr) sh.load(y_sh + t * d + (int64_t)v * 8);
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          if (j >= k || dj[j] < 0) continue;
+          float f[8];
+          val[j].to_float(f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[j], f[i], acc[i]);
+        }
+        if (y_sh != nullptr) {
+          float f[8];
+          sh.to_float(f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] += f[i];
+        }
+        Vec8<T> out;
+        out.from_float(acc);
+        out.store(y + t * d + (int64_t)v * 8);
+      }
+    } else {
+    // general k (and the router term): one row at a time
     // uniform across the warp: every lane takes part in every shuffle; accesses predicated
     for (int vb = 0; vb < nvec; vb += 32) {
       const int v = vb + lane;
@@ -276,6 +316,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
         out.from_float(acc);
         out.store(y + t * d + (int64_t)v * 8);
       }
+    }
     }
   }
 }
@@ -346,27 +387,34 @@ cudaError_t launch_permute_rows(const void* x, const int32_t* dest, const moe_di
   return cudaGetLastError();
 }
 
+namespace {
+template <typename T>
+void combine_dispatch(const T* y_perm, const int32_t* dest, const float* topk_w, const T* y_sh,
+                      const int32_t* idx, const float* dl_tok, const float* w_rT, const moe_dims& dm,
+                      T* y, unsigned blocks, cudaStream_t st) {
+  if (w_rT != nullptr)
+    combine_kernel<T, true, 0><<<blocks, 256, 0, st>>>(y_perm, dest, topk_w, y_sh, idx, dl_tok, w_rT, dm.T,
+                                                       dm.d, dm.k, y);
+  else if (dm.k <= 8)
+    combine_kernel<T, false, 8><<<blocks, 256, 0, st>>>(y_perm, dest, topk_w, y_sh, idx, dl_tok, w_rT, dm.T,
+                                                        dm.d, dm.k, y);
+  else
+    combine_kernel<T, false, 0><<<blocks, 256, 0, st>>>(y_perm, dest, topk_w, y_sh, idx, dl_tok, w_rT, dm.T,
+                                                        dm.d, dm.k, y);
+}
+}  // namespace
+
 cudaError_t launch_combine(const void* y_perm, const int32_t* dest, const float* topk_w,
                            const void* y_sh, const int32_t* idx, const float* dl_tok,
                            const float* w_rT, const moe_dims& dm, void* y, cudaStream_t st) {
   const unsigned blocks = (unsigned)token_blocks(dm.T, 8, 1 << 20);
-  const bool router = w_rT != nullptr;
   TraceScope ts(topk_w != nullptr ? TP_COMBINE : TP_COMBINE_BWD, st);
-  if (dm.dtype == MOE_F32) {
-    if (router)
-      combine_kernel<float, true><<<blocks, 256, 0, st>>>((const float*)y_perm, dest, topk_w,
-          (const float*)y_sh, idx, dl_tok, w_rT, dm.T, dm.d, dm.k, (float*)y);
-    else
-      combine_kernel<float, false><<<blocks, 256, 0, st>>>((const float*)y_perm, dest, topk_w,
-          (const float*)y_sh, idx, dl_tok, w_rT, dm.T, dm.d, dm.k, (float*)y);
-  } else {
-    if (router)
-      combine_kernel<__nv_bfloat16, true><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y_perm, dest,
-          topk_w, (const __nv_bfloat16*)y_sh, idx, dl_tok, w_rT, dm.T, dm.d, dm.k, (__nv_bfloat16*)y);
-    else
-      combine_kernel<__nv_bfloat16, false><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)y_perm, dest,
-          topk_w, (const __nv_bfloat16*)y_sh, idx, dl_tok, w_rT, dm.T, dm.d, dm.k, (__nv_bfloat16*)y);
-  }
+  if (dm.dtype == MOE_F32)
+    combine_dispatch<float>((const float*)y_perm, dest, topk_w, (const float*)y_sh, idx, dl_tok, w_rT, dm,
+                            (float*)y, blocks, st);
+  else
+    combine_dispatch<__nv_bfloat16>((const __nv_bfloat16*)y_perm, dest, topk_w, (const __nv_bfloat16*)y_sh,
+                                    idx, dl_tok, w_rT, dm, (__nv_bfloat16*)y, blocks, st);
   return cudaGetLastError();
 }
 
