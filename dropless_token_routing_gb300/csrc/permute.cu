@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const T* __restrict__
 
 // ---------------------------------------------------------------- a4: combine
 // y[t] = sum_j w_j y_perm[dest_j] (+ y_sh[t]) (+ sum_j dl_j W_r^T[e_j]) in fp32, in that
-// order, rounded once. One warp per token, 8 elements per lane per step. With k <= KMAX the
+// order, rounded once, 8 elements per lane per step. With k <= KMAX (no router term) the
 // k rows' vectors of a step (and the shared expert's) are all requested before the sums
 // start, so a warp keeps k + 1 loads in flight instead of one; the sums keep their order.
 template <typename T, bool ROUTER, int KMAX>
@@ -224,31 +224,35 @@ __global__ void __launch_bounds__(256) combine_kernel(
     const float* __restrict__ w_rT, int64_t Tn, int d, int k, T* __restrict__ y) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int nvec = d / 8;
-  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < Tn; t += (int64_t)gridDim.x * nw) {
-    int dq = -1, eq = 0;
-    float wq = 0.f, gq = 0.f;
-    if (lane < k) {
-      const int64_t q = t * k + lane;
-      dq = dest[q];
-      wq = topk_w != nullptr ? topk_w[q] : 1.f;
-      if (ROUTER) {
-        eq = idx[q];
-        gq = dl_tok[q];
+  if constexpr (KMAX > 0) {
+    // A warp's unit of work is one segment of up to kSegVec vectors of one token's row, so
+    // that short rows still give every SM enough warps (and loads) in flight.
+    constexpr int kSegVec = 128;
+    const int nseg = (nvec + kSegVec - 1) / kSegVec;
+    const int64_t items = Tn * nseg;
+    for (int64_t it = (int64_t)blockIdx.x * nw + warp; it < items; it += (int64_t)gridDim.x * nw) {
+      const int64_t t = it / nseg;
+      const int seg = (int)(it - t * nseg);
+      int dq = -1;
+      float wq = 0.f;
+      if (lane < k) {
+        const int64_t q = t * k + lane;
+        dq = dest[q];
+        wq = topk_w != nullptr ? topk_w[q] : 1.f;
       }
-    }
-    if constexpr (KMAX > 0) {
       // every lane holds every copy's row and weight (uniform across the warp)
-      int dj[KMAX > 0 ? KMAX : 1];
-      float wj[KMAX > 0 ? KMAX : 1];
+      int dj[KMAX];
+      float wj[KMAX];
 #pragma unroll
       for (int j = 0; j < KMAX; ++j) {
         dj[j] = __shfl_sync(0xffffffffu, dq, j);
         wj[j] = __shfl_sync(0xffffffffu, wq, j);
       }
-      for (int vb = 0; vb < nvec; vb += 32) {
+      const int vend = min(nvec, (seg + 1) * kSegVec);
+      for (int vb = seg * kSegVec; vb < vend; vb += 32) {
         const int v = vb + lane;
-        if (v >= nvec) break;        // no shuffles below: lanes may leave
-        Vec8<T> val[KMAX > 0 ? KMAX : 1], sh;
+        if (v >= vend) break;        // no shuffles below: lanes may leave
+        Vec8<T> val[KMAX], sh;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j)
           if (j < k && dj[j] >= 0) val[j].load(y_perm + (int64_t)dj[j] * d + (int64_t)v * 8);
@@ -272,51 +276,64 @@ __global__ void __launch_bounds__(256) combine_kernel(
         out.from_float(acc);
         out.store(y + t * d + (int64_t)v * 8);
       }
-    } else {
-    // general k (and the router term): one row at a time
-    // uniform across the warp: every lane takes part in every shuffle; accesses predicated
-    for (int vb = 0; vb < nvec; vb += 32) {
-      const int v = vb + lane;
-      const bool on = v < nvec;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int j = 0; j < k; ++j) {
-        const int dj = __shfl_sync(0xffffffffu, dq, j);
-        const float wj = __shfl_sync(0xffffffffu, wq, j);
-        if (dj < 0 || !on) continue;
-        Vec8<T> val;
-        val.load(y_perm + (int64_t)dj * d + (int64_t)v * 8);
-        float f[8];
-        val.to_float(f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
-      }
-      if (y_sh != nullptr && on) {
-        Vec8<T> val;
-        val.load(y_sh + t * d + (int64_t)v * 8);
-        float f[8];
-        val.to_float(f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += f[i];
-      }
-      if (ROUTER) {
-        for (int j = 0; j < k; ++j) {
-          const int ej = __shfl_sync(0xffffffffu, eq, j);
-          const float gj = __shfl_sync(0xffffffffu, gq, j);
-          if (!on) continue;
-          const float4* wr = reinterpret_cast<const float4*>(w_rT + (int64_t)ej * d + (int64_t)v * 8);
-          const float4 p0 = __ldg(wr), p1 = __ldg(wr + 1);
-          acc[0] = fmaf(gj, p0.x, acc[0]); acc[1] = fmaf(gj, p0.y, acc[1]);
-          acc[2] = fmaf(gj, p0.z, acc[2]); acc[3] = fmaf(gj, p0.w, acc[3]);
-          acc[4] = fmaf(gj, p1.x, acc[4]); acc[5] = fmaf(gj, p1.y, acc[5]);
-          acc[6] = fmaf(gj, p1.z, acc[6]); acc[7] = fmaf(gj, p1.w, acc[7]);
+    }
+  } else {
+    // general k (and the router term): one token per warp, one row at a time
+    for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < Tn; t += (int64_t)gridDim.x * nw) {
+      int dq = -1, eq = 0;
+      float wq = 0.f, gq = 0.f;
+      if (lane < k) {
+        const int64_t q = t * k + lane;
+        dq = dest[q];
+        wq = topk_w != nullptr ? topk_w[q] : 1.f;
+        if (ROUTER) {
+          eq = idx[q];
+          gq = dl_tok[q];
         }
       }
-      if (on) {
-        Vec8<T> out;
-        out.from_float(acc);
-        out.store(y + t * d + (int64_t)v * 8);
+      // uniform across the warp: every lane takes part in every shuffle; accesses predicated
+      for (int vb = 0; vb < nvec; vb += 32) {
+        const int v = vb + lane;
+        const bool on = v < nvec;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < k; ++j) {
+          const int dj = __shfl_sync(0xffffffffu, dq, j);
+          const float wj = __shfl_sync(0xffffffffu, wq, j);
+          if (dj < 0 || !on) continue;
+          Vec8<T> val;
+          val.load(y_perm + (int64_t)dj * d + (int64_t)v * 8);
+          float f[8];
+          val.to_float(f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+        }
+        if (y_sh != nullptr && on) {
+          Vec8<T> val;
+          val.load(y_sh + t * d + (int64_t)v * 8);
+          float f[8];
+          val.to_float(f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] += f[i];
+        }
+        if (ROUTER) {
+          for (int j = 0; j < k; ++j) {
+            const int ej = __shfl_sync(0xffffffffu, eq, j);
+            const float gj = __shfl_sync(0xffffffffu, gq, j);
+            if (!on) continue;
+            const float4* wr = reinterpret_cast<const float4*>(w_rT + (int64_t)ej * d + (int64_t)v * 8);
+            const float4 p0 = __ldg(wr), p1 = __ldg(wr + 1);
+            acc[0] = fmaf(gj, p0.x, acc[0]); acc[1] = fmaf(gj, p0.y, acc[1]);
+            acc[2] = fmaf(gj, p0.z, acc[2]); acc[3] = fmaf(gj, p0.w, acc[3]);
+            acc[4] = fmaf(gj, p1.x, acc[4]); acc[5] = fmaf(gj, p1.y, acc[5]);
+            acc[6] = fmaf(gj, p1.z, acc[6]); acc[7] = fmaf(gj, p1.w, acc[7]);
+          }
+        }
+        if (on) {
+          Vec8<T> out;
+          out.from_float(acc);
+          out.store(y + t * d + (int64_t)v * 8);
+        }
       }
-    }
     }
   }
 }
@@ -407,7 +424,9 @@ void combine_dispatch(const T* y_perm, const int32_t* dest, const float* topk_w,
 cudaError_t launch_combine(const void* y_perm, const int32_t* dest, const float* topk_w,
                            const void* y_sh, const int32_t* idx, const float* dl_tok,
                            const float* w_rT, const moe_dims& dm, void* y, cudaStream_t st) {
-  const unsigned blocks = (unsigned)token_blocks(dm.T, 8, 1 << 20);
+  // one warp per row segment of 128 vectors (general path: per token), eight warps a block
+  const int64_t nseg = (dm.d / 8 + 127) / 128;
+  const unsigned blocks = (unsigned)token_blocks(dm.T * nseg, 8, 1 << 20);
   TraceScope ts(topk_w != nullptr ? TP_COMBINE : TP_COMBINE_BWD, st);
   if (dm.dtype == MOE_F32)
     combine_dispatch<float>((const float*)y_perm, dest, topk_w, (const float*)y_sh, idx, dl_tok, w_rT, dm,
