@@ -37,11 +37,14 @@ UNIT = "tokens/s"
 # DRAM traffic per launch from an ncu capture of the dominant kernel, keyed by the phase
 # name; valid only while the kernel source still hashes to src_sha256.
 NCU_TRAFFIC = {
-    # ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum (one pass)
-    # on the default workload, one launch after warm-up; see profiles/gemm_dw13_pangu_bf16.md.
+    # ncu --set full (with dram__bytes_read.sum / dram__bytes_write.sum) on the small case
+    # T=1024, E=32 (33 gradient groups, 9216 token-copy rows), one launch after warm-up, scaled
+    # to the full workload by the units each term grows with: reads by the token-copy rows
+    # (73728 / 9216), writes by the gradient groups (257 / 33). Small case: 217.2 MB read,
+    # 2016.7 MB written; scaled: 1737.9 MB + 15705.6 MB. See profiles/gemm_dw13_pangu_bf16.md.
     # Applies only while the kernel's source file is unchanged since the capture.
     "gemm_dw13": {"src": "gemm_tc_pair.cu", "workload": "pangu_bf16",
-                  "bytes_per_launch": 2142385664 + 16162899968,
+                  "bytes_per_launch": 1737900000 + 15705600000,
                   "src_sha256": "b484dbad13ab9eef2403ff3d6ffe33d418134fb55fc8bcf4c9bb6d363dd7375f"},
 }
 
@@ -570,7 +573,10 @@ def main():
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
-        time.sleep(0.3)
+        t_wait = time.time()
+        while not sampler.lines and time.time() - t_wait < 5.0:   # nvidia-smi has started
+            time.sleep(0.05)
+        time.sleep(0.2)
     N.trace_enable(True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
