@@ -37,7 +37,6 @@ using namespace tc;
 
 struct TcParams {
   CUtensorMap a0, a1, b0, b1;
-  CUtensorMap g0;      // row gather of the routed A operand (x or dy, box {64, 1})
   GroupedArgs g;
 };
 
@@ -72,6 +71,24 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v)
   }
 }
 
+// Fused rearrangement: the 128 x 64 A tile of K block kb, gathered from the token rows `tok`
+// (lane L holds the tokens of tile rows 4i + L/8, i = 0..31) with 16-byte cp.async in the
+// TMA's 128-byte swizzled layout (16-byte chunk c of row r at chunk c ^ (r & 7)). Each
+// instruction of the warp copies four whole 128-byte row segments. The copies complete on
+// `bar` (cp.async.mbarrier.arrive); the LSU path is not bound by the TMA unit's rate per
+// instruction, which 512-byte tile::gather4 copies are (about 5 B/cycle per SM).
+__device__ __forceinline__ void gather_a_tile(uint32_t a_s, const __nv_bfloat16* src, int d, int kb,
+                                              const int (&tok)[32], int lane, uint32_t bar) {
+  const int c = lane & 7;
+  const __nv_bfloat16* s0 = src + kb * BK + 8 * c;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    cp_async16(a_s + r * 128 + ((c ^ (r & 7)) << 4), s0 + (int64_t)tok[i] * d);
+  }
+  cp_async_arrive(bar);
+}
+
 template <int MODE> struct ModeTraits {
   static constexpr bool b_mn = (MODE == BWD2T || MODE == BWD1T);
   static constexpr int bn_eff = (MODE == FWD1) ? BN / 2 : BN;
@@ -79,7 +96,7 @@ template <int MODE> struct ModeTraits {
 
 // ------------------------------------------------------------------ producer: TMA issue
 // `gather`: the routed A tile is gathered row by row by the whole producer warp instead
-// (tma_gather4 in the producer loop), so it is skipped here.
+// (gather_a_tile), so it is skipped here.
 template <int MODE>
 __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCoord& tc, int kb,
                                                  uint32_t a_s, uint32_t b_s, uint32_t bar, bool gather) {
@@ -403,14 +420,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     for (TileCursor cur(sched, ng, blockIdx.x, gridDim.x); cur.valid() && ok; cur.advance()) {
       const TileCoord tc = cur.coord(a, MODE, BM, s_off);
       const int nkb = (tc.G.K + BK - 1) / BK;
-      // fused rearrangement: lane j gathers tile rows 4j..4j+3 (rows past the segment repeat
-      // its first row; they are computed but never stored)
+      // fused rearrangement: lane L gathers chunk L % 8 of tile rows 4i + L / 8 (rows past the
+      // segment repeat its first row; they are computed but never stored)
       const bool gather = (MODE == FWD1 || MODE == BWD2T) && a.gather_rows != nullptr && !tc.G.shared;
-      int tok[4] = {0, 0, 0, 0};
+      int tok[32];
       if (gather) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int m = tc.mi * BM + 4 * lane + i;
+        for (int i = 0; i < 32; ++i) {
+          const int m = tc.mi * BM + 4 * i + (lane >> 3);
           tok[i] = __ldg(a.gather_rows + tc.G.row0 + (m < tc.G.M ? m : 0));
         }
       }
@@ -420,13 +437,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
         const uint32_t bar = smem_u32(&full_bar[stage]);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar, STAGE_BYTES);
-          issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, bar, gather);
-        }
         if (gather) {
+          // every lane's copies are counted by the barrier before the expect-tx arrival below
+          gather_a_tile(a_s, (const __nv_bfloat16*)(MODE == FWD1 ? a.x : a.dy), a.d, kb, tok, lane, bar);
           __syncwarp();
-          tma_gather4(a_s + 512 * lane, &p.g0, bar, kb * BK, tok[0], tok[1], tok[2], tok[3]);
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, gather ? B_BYTES : STAGE_BYTES);
+          issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, bar, gather);
         }
         pending |= 1u << stage;
         pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
@@ -449,6 +467,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
         const TileCoord tc = cur.coord(a, MODE, BM, s_off);
         const int nkb = (tc.G.K + BK - 1) / BK;
         const int b = it & 1;
+        // a gathered A tile was written through the generic proxy (cp.async): order it before
+        // the tensor core's reads
+        const bool gathered = (MODE == FWD1 || MODE == BWD2T) && a.gather_rows != nullptr && !tc.G.shared;
         if (!mbar_wait_bounded(smem_u32(&tempty_bar[b]), ((it >> 1) & 1) ^ 1, &abort_flag, a.err,
                                kWaitLimitNs)) break;
         tc_fence_after();
@@ -456,6 +477,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&full_bar[stage]), phase, &abort_flag, a.err,
                                  kWaitLimitNs)) { ok = false; break; }
+          if (gathered) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_after();
           const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
 #pragma unroll
@@ -544,7 +566,7 @@ int launch_tc_grouped(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
   const bool sh = g.S > 0;
   switch (mode) {
     case FWD1:
-      ok = (g.gather_rows != nullptr ? map2d(&p.g0, g.x, d, T, 64, 1) : map2d(&p.a0, g.x_perm, d, Tk, 64, 128)) &&
+      ok = (g.gather_rows != nullptr || map2d(&p.a0, g.x_perm, d, Tk, 64, 128)) &&
            map3d(&p.b0, g.w13, d, 2 * f, E, 64, 128);
       if (sh) ok = ok && map2d(&p.a1, g.x, d, T, 64, 128) && map3d(&p.b1, g.ws13, d, 2 * fs, S, 64, 128);
       if (!ok) return MOE_ERR_CUDA;
@@ -555,7 +577,7 @@ int launch_tc_grouped(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<FWD2>(p, num_sms, st);
     case BWD2T:
-      ok = (g.gather_rows != nullptr ? map2d(&p.g0, g.dy, d, T, 64, 1) : map2d(&p.a0, g.dy_perm, d, Tk, 64, 128)) &&
+      ok = (g.gather_rows != nullptr || map2d(&p.a0, g.dy_perm, d, Tk, 64, 128)) &&
            map3d(&p.b0, g.w2, f, d, E, 64, 64);
       if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 128) && map3d(&p.b1, g.ws2, fs, d, S, 64, 64);
       if (!ok) return MOE_ERR_CUDA;

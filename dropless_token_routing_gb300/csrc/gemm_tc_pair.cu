@@ -61,7 +61,6 @@ constexpr int SLAB = 64 * 128;          // one 64-element-wide, 64-row swizzled 
 
 struct PairParams {
   CUtensorMap a0, a1, b0, b1;  // operands (routed / shared), box {64, 64}
-  CUtensorMap g0;              // row gather of the routed token operand (dy or x, box {64, 1})
   CUtensorMap o0, o1;          // dW outputs (routed / shared), box {64, 32, 1}
   GroupedArgs g;
 };
@@ -119,7 +118,7 @@ __device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
 // This CTA's halves of K block kb: A = output rows [m0, m0+128), B = output columns
 // [n0, n0+128), both MN-major (the token copies run along K). `gather`: the token operand
 // (A = dY for dW2, B = x for dW13) is gathered by the whole producer warp instead
-// (issue_gather_half), so it is skipped here.
+// (gather_token_half), so it is skipped here.
 template <int MODE>
 __device__ __forceinline__ void issue_half_loads(const PairParams& p, const TileCoord& tc, int kb,
                                                  uint32_t rank, uint32_t a_s, uint32_t b_s,
@@ -144,25 +143,41 @@ __device__ __forceinline__ void issue_half_loads(const PairParams& p, const Tile
   }
 }
 
-// Fused rearrangement of the token operand of a routed group: lane j fills rows
-// 4(j%16)..4(j%16)+3 of 64-column slab j/16 with the tokens of those permuted rows (rows
-// past the segment repeat its first row: the ragged K fix-up zeroes the matching A rows, so
-// they add nothing).
+// Fused rearrangement of the token operand of a routed group (dY for dW2, x for dW13): this
+// CTA's 128 columns of the K block's 64 token rows are gathered from the token-order tensor
+// with 16-byte cp.async (one 64-column slab = 128 bytes per row, in the TMA's 128-byte
+// swizzled layout: chunk c of row k at chunk c ^ (k & 7)). Per instruction the warp copies
+// two rows x 256 bytes; rows past the segment repeat its first row (the ragged K fix-up
+// zeroes the matching A rows, so they add nothing), and columns past the tensor are zero
+// filled. The copies complete on `bar`. (TMA tile::gather4 copies of 512 bytes are held to
+// about 5 B/cycle per SM by the TMA unit's rate per instruction.)
 template <int MODE>
-__device__ __forceinline__ void issue_gather_half(const PairParams& p, const TileCoord& tc, int kb,
+__device__ __forceinline__ void gather_token_half(const PairParams& p, const TileCoord& tc, int kb,
                                                   uint32_t rank, uint32_t a_s, uint32_t b_s,
                                                   uint32_t bar, int lane) {
   const GroupGeom& G = tc.G;
-  const int sl = lane >> 4, q = lane & 15;
-  int tok[4];
+  const int d = p.g.d;
+  const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(MODE == DW13 ? p.g.x : p.g.dy);
+  // this lane's token rows: lane and lane + 32 of the K block
+  int tk[2];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int k = kb * BK + 4 * q + i;
-    tok[i] = __ldg(p.g.gather_rows + G.row0 + (k < G.K ? k : 0));
+  for (int h = 0; h < 2; ++h) {
+    const int k = kb * BK + lane + 32 * h;
+    tk[h] = __ldg(p.g.gather_rows + G.row0 + (k < G.K ? k : 0));
   }
-  const int c0 = MODE == DW13 ? tc.ni * BN + HN * (int)rank : tc.mi * PM + HM * (int)rank;
-  const uint32_t dst = (MODE == DW13 ? b_s : a_s) + sl * SLAB + q * 512;
-  tma_gather4(dst, &p.g0, bar, c0 + 64 * sl, tok[0], tok[1], tok[2], tok[3]);
+  const int c0 = (MODE == DW13 ? tc.ni * BN + HN * (int)rank : tc.mi * PM + HM * (int)rank);
+  const int sl = (lane >> 3) & 1, c = lane & 7;
+  const int col = c0 + 64 * sl + 8 * c;                 // this lane's 8 columns
+  const bool col_ok = col < d;                          // d is a multiple of 64
+  const uint32_t dst0 = (MODE == DW13 ? b_s : a_s) + sl * SLAB;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int k = 2 * i + (lane >> 4);                  // K row of this copy
+    const int t = __shfl_sync(0xffffffffu, i < 16 ? tk[0] : tk[1], k & 31);
+    const __nv_bfloat16* g = src + (int64_t)t * d + (col_ok ? col : 0);
+    cp_async16(dst0 + k * 128 + ((c ^ (k & 7)) << 4), g, col_ok ? 16u : 0u);
+  }
+  cp_async_arrive(bar);
 }
 
 // ------------------------------------------------------------------ epilogue
@@ -291,13 +306,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
         const uint32_t bar = smem_u32(&land_bar[stage]);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar, STAGE_BYTES);
-          issue_half_loads<MODE>(p, tc, kb, rank, a_s, b_s, bar, gather);
-        }
         if (gather) {
+          // every lane's copies are counted by the barrier before the expect-tx arrival below
+          gather_token_half<MODE>(p, tc, kb, rank, a_s, b_s, bar, lane);
           __syncwarp();
-          issue_gather_half<MODE>(p, tc, kb, rank, a_s, b_s, bar, lane);
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar, gather ? STAGE_BYTES - (MODE == DW13 ? B_BYTES : A_BYTES) : STAGE_BYTES);
+          issue_half_loads<MODE>(p, tc, kb, rank, a_s, b_s, bar, gather);
         }
         pending |= 1u << stage;
         pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
@@ -317,6 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
       const TileCoord tc = cur.coord(a, MODE, PM, s_off);
       const int nkb = (tc.G.K + BK - 1) / BK;
       const int w = it & 1;   // the issuer of this tile
+      const bool gathered = a.gather_rows != nullptr && !tc.G.shared;
       for (int kb = 0; kb < nkb; ++kb) {
         const bool got = mbar_wait_bounded(smem_u32(&land_bar[stage]), phase, &abort_flag, a.err,
                                            kWaitLimitNs);
@@ -331,6 +348,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
             const int sl = i / per_slab, j = i - sl * per_slab;
             A4[sl * (SLAB / 16) + rem * 8 + j] = make_uint4(0u, 0u, 0u, 0u);
           }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        } else if (gathered) {
+          // the gathered half was written through the generic proxy (cp.async)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
         __syncwarp();
@@ -481,7 +501,7 @@ int launch_tc_pair_dw(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
   bool ok;
   const bool gather = g.gather_rows != nullptr;
   if (mode == DW2) {
-    ok = (gather ? map2d(&p.g0, g.dy, d, T, 64, 1) : map2d(&p.a0, g.dy_perm, d, Tk, 64, 64)) &&
+    ok = (gather || map2d(&p.a0, g.dy_perm, d, Tk, 64, 64)) &&
          map2d(&p.b0, g.hw, f, Tk, 64, 64) && map3d(&p.o0, g.dw2, f, d, E, 64, 32);
     if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 64) && map2d(&p.b1, g.hw_sh, fs, ST, 64, 64) &&
                  map3d(&p.o1, g.dws2, fs, d, S, 64, 32);
@@ -489,7 +509,7 @@ int launch_tc_pair_dw(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
     return launch_pair<DW2>(p, num_sms, st);
   }
   ok = map2d(&p.a0, g.dz, 2 * f, Tk, 64, 64) &&
-       (gather ? map2d(&p.g0, g.x, d, T, 64, 1) : map2d(&p.b0, g.x_perm, d, Tk, 64, 64)) &&
+       (gather || map2d(&p.b0, g.x_perm, d, Tk, 64, 64)) &&
        map3d(&p.o0, g.dw13, d, 2 * f, E, 64, 32);
   if (sh) ok = ok && map2d(&p.a1, g.dz_sh, 2 * fs, ST, 64, 64) && map2d(&p.b1, g.x, d, T, 64, 64) &&
                map3d(&p.o1, g.dws13, d, 2 * fs, S, 64, 32);

@@ -1,5 +1,5 @@
 // PTX wrappers and tensor-map helpers shared by the tcgen05 GEMM kernels: TMA tensor
-// loads and stores, bulk-group waits, tcgen05 fences, shared-memory matrix and instruction
+// loads and stores, 16-byte cp.async row copies, bulk-group waits, tcgen05 fences, shared-memory matrix and instruction
 // descriptors, TMEM loads, bf16 packing, and cuTensorMapEncodeTiled reached through the
 // runtime's driver entry point.
 #pragma once
@@ -29,15 +29,15 @@ __device__ __forceinline__ void tma3d(uint32_t dst, const CUtensorMap* map, uint
       : "memory");
 }
 
-// Four rows (r0..r3) of a 2-D map whose box is one row high, each `box` columns wide from
-// column c0, land as consecutive rows at dst (with the map's swizzle): a row gather.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
-                                            int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-      : "memory");
+// 16 bytes global -> shared through the LSU (L2 only); `bytes` < 16 zero-fills the rest
+// (0: nothing is read).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes = 16) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+// Arrive on an mbarrier once every cp.async this thread issued before has landed (the
+// barrier's pending count is raised at once, so the phase waits for these copies).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void tma_store3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
