@@ -506,6 +506,8 @@ def main():
                                 + (f"(s={cfg['zipf_s']})" if cfg['routing'] == 'zipf' else ""),
                     "tokens_per_step": T, "l2": "inputs larger than L2 (expert weights > 20 GB)",
                     "parallelism": f"replicas x{world}"}
+    if world > 1:
+        workload_cfg["replicas"] = "data parallel: the same weights, each rank its own seeded tokens"
 
     if args.impl == "reference":
         if rank != 0:
@@ -542,7 +544,7 @@ def main():
     from dropless_token_routing_gb300.api import LayerParams, MoELayer, get_device_error
 
     dev = torch.device("cuda", torch.cuda.current_device())
-    w = make_workload(cfg, device=dev)
+    w = make_workload(cfg, device=dev, replica=rank)   # data parallel: each rank its own tokens
     params = LayerParams(w13=w.w13, w2=w.w2, w_r=w.w_r, bias=w.bias, ws13=w.ws13, ws2=w.ws2)
     gather = args.rearrange == "gather"
     layer = MoELayer(params, T, cfg["d"], cfg["E"], cfg["k"], cfg["f"], cfg["S"], cfg["f_s"],

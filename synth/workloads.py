@@ -31,6 +31,11 @@ Recipe (every draw is seeded; seed = workload index, the tiny one is seed 0):
   straddling the top-k boundary) and in a further ceil(0.005 * T) rows the 3rd
   largest is overwritten with the 2nd (a tie inside the top-k).
 
+Replicas (one per rank of a multi-GPU run, data parallel): replica 0 is the draw
+above; replica r > 0 keeps its weights, router and bias, and draws its own token
+side (``x``, ``dY`` and, for the adversarial workload, the logit construction)
+from a second generator seeded with ``seed + REPLICA_SEED_STRIDE * r``.
+
 Expert weight layouts are K-major: ``W13 [E][2f][d]`` (gate rows ``0..f-1``,
 up rows ``f..2f-1``), ``W2 [E][d][f]``; the shared experts use the same
 layouts ``Ws13 [S][2f_s][d]``, ``Ws2 [S][d][f_s]``.
@@ -62,6 +67,7 @@ BOUNDARY_TIE_FRACTION = 0.01
 INNER_TIE_FRACTION = 0.005
 DEAD_LOGIT = -30.0
 WEIGHT_STD = 0.02
+REPLICA_SEED_STRIDE = 7919
 
 
 def shrink(name: str, **overrides) -> dict:
@@ -147,8 +153,9 @@ def _adversarial_logits(g, T, E, k, device):
     return base, info
 
 
-def make_workload(cfg, device="cpu", with_dy: bool = True) -> Workload:
-    """Draw the inputs of one workload.  ``cfg`` is a name of CONFIGS or a dict."""
+def make_workload(cfg, device="cpu", with_dy: bool = True, replica: int = 0) -> Workload:
+    """Draw the inputs of one workload.  ``cfg`` is a name of CONFIGS or a dict.
+    ``replica`` > 0: the same weights with that replica's own token batch."""
     if isinstance(cfg, str):
         cfg = dict(CONFIGS[cfg], name=cfg)
     cfg = dict(cfg)
@@ -175,5 +182,12 @@ def make_workload(cfg, device="cpu", with_dy: bool = True) -> Workload:
     logits_in = None
     if cfg["routing"] == "adversarial":
         logits_in, info = _adversarial_logits(g, T, E, k, device)
+    if replica > 0:
+        gr = torch.Generator(device=device)
+        gr.manual_seed(int(cfg["seed"]) + REPLICA_SEED_STRIDE * int(replica))
+        x = _normal(gr, (T, d), 1.0, device, dt)
+        dy = _normal(gr, (T, d), 1.0, device, dt) if with_dy else None
+        if cfg["routing"] == "adversarial":
+            logits_in, info = _adversarial_logits(gr, T, E, k, device)
     return Workload(cfg=cfg, x=x, w_r=w_r, bias=bias, w13=w13, w2=w2, ws13=ws13, ws2=ws2,
                     dy=dy, logits_in=logits_in, info=info)

@@ -41,3 +41,20 @@ def test_adversarial_construction():
         srt = np.sort(L[t])[::-1]
         assert srt[1] == srt[2]
     assert len(w.info["boundary_tie_rows"]) == math.ceil(0.01 * T)
+
+
+def test_replicas_share_weights_and_draw_their_own_tokens():
+    """Replica 0 is the plain draw; replica r > 0 keeps every weight and draws its own x, dY
+    (and adversarial logits) from its own seed."""
+    import torch
+    cfg = shrink("pangu_bf16", T=32, d=64, E=16, k=4, f=64, f_s=64)
+    a, a0, b = make_workload(cfg), make_workload(cfg, replica=0), make_workload(cfg, replica=1)
+    for n in ("x", "dy", "w13", "w2", "ws13", "ws2", "w_r", "bias"):
+        assert torch.equal(getattr(a, n), getattr(a0, n)), n
+    for n in ("w13", "w2", "ws13", "ws2", "w_r", "bias"):
+        assert torch.equal(getattr(a, n), getattr(b, n)), n
+    assert not torch.equal(a.x, b.x) and not torch.equal(a.dy, b.dy)
+    adv = shrink("adversarial_bf16", T=64, d=64, E=32, k=8, f=64, f_s=64)
+    c, d = make_workload(adv), make_workload(adv, replica=2)
+    assert torch.equal(c.w13, d.w13) and not torch.equal(c.logits_in, d.logits_in)
+    assert d.info["n_hot_rows"] == c.info["n_hot_rows"]
