@@ -37,15 +37,15 @@ UNIT = "tokens/s"
 # DRAM traffic per launch from an ncu capture of the dominant kernel, keyed by the phase
 # name; valid only while the kernel source still hashes to src_sha256.
 NCU_TRAFFIC = {
-    # ncu --set full (with dram__bytes_read.sum / dram__bytes_write.sum) on the small case
-    # T=1024, E=32 (33 gradient groups, 9216 token-copy rows), one launch after warm-up, scaled
-    # to the full workload by the units each term grows with: reads by the token-copy rows
-    # (73728 / 9216), writes by the gradient groups (257 / 33). Small case: 217.2 MB read,
-    # 2016.7 MB written; scaled: 1737.9 MB + 15705.6 MB. See profiles/gemm_dw13_pangu_bf16.md.
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the small case T=1024, E=32
+    # (33 gradient groups, 9216 token-copy rows), one launch after warm-up, scaled to the full
+    # workload by the units each term grows with: reads by the token-copy rows (73728 / 9216),
+    # writes by the gradient groups (257 / 33). Small case: 217.3 MB read, 2016.8 MB
+    # written; scaled: 1738.1 MB + 15706.9 MB. See profiles/gemm_dw13_pangu_bf16.md.
     # Applies only while the kernel's source file is unchanged since the capture.
     "gemm_dw13": {"src": "gemm_tc_pair.cu", "workload": "pangu_bf16",
-                  "bytes_per_launch": 1737900000 + 15705600000,
-                  "src_sha256": "b484dbad13ab9eef2403ff3d6ffe33d418134fb55fc8bcf4c9bb6d363dd7375f"},
+                  "bytes_per_launch": 1738100736 + 15706855114,
+                  "src_sha256": "4d3282dbecfc04147ec34c5a9ac50b4ee4e365651108b6e6c283db9868284cf6"},
 }
 
 
