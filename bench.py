@@ -41,11 +41,11 @@ NCU_TRAFFIC = {
     # (33 gradient groups, 9216 token-copy rows), one launch after warm-up, scaled to the full
     # workload by the units each term grows with: reads by the token-copy rows (73728 / 9216),
     # writes by the gradient groups (257 / 33). Small case: 217.3 MB read, 2016.8 MB
-    # written; scaled: 1738.1 MB + 15706.9 MB. See profiles/gemm_dw13_pangu_bf16.md.
+    # written; scaled: 1738.1 MB + 15706.4 MB. See profiles/gemm_dw13_pangu_bf16.md.
     # Applies only while the kernel's source file is unchanged since the capture.
     "gemm_dw13": {"src": "gemm_tc_pair.cu", "workload": "pangu_bf16",
-                  "bytes_per_launch": 1738100736 + 15706855114,
-                  "src_sha256": "4d3282dbecfc04147ec34c5a9ac50b4ee4e365651108b6e6c283db9868284cf6"},
+                  "bytes_per_launch": 1738119168 + 15706380614,
+                  "src_sha256": "ebe602d5efffe650047c60502e590f7caf250704f798b6ee5f00a6f3ca2f5095"},
 }
 
 

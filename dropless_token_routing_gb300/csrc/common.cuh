@@ -105,6 +105,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+// Raise the phase's expected transaction bytes without arriving (the arrival comes later).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
 
 // Wait for the phase with the given parity to complete, for at most limit_ns nanoseconds.
 // Gives up early when *abort becomes non-zero (another role of the CTA already failed).

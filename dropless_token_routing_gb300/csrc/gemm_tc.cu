@@ -438,13 +438,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
         const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
         const uint32_t bar = smem_u32(&full_bar[stage]);
         if (gather) {
-          // every lane's copies are counted by the barrier before the expect-tx arrival below
+          // the weight tile's TMA first; lane 0 arrives only after every lane's copies are
+          // counted by the barrier
+          if (lane == 0) {
+            mbar_expect_tx(bar, B_BYTES);
+            issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, bar, true);
+          }
           gather_a_tile(a_s, (const __nv_bfloat16*)(MODE == FWD1 ? a.x : a.dy), a.d, kb, tok, lane, bar);
           __syncwarp();
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar, gather ? B_BYTES : STAGE_BYTES);
-          issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, bar, gather);
+          if (lane == 0) mbar_arrive(bar);
+        } else if (lane == 0) {
+          mbar_arrive_expect_tx(bar, STAGE_BYTES);
+          issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, bar, false);
         }
         pending |= 1u << stage;
         pend_par = (pend_par & ~(1u << stage)) | (phase << stage);

@@ -307,13 +307,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
         const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
         const uint32_t bar = smem_u32(&land_bar[stage]);
         if (gather) {
-          // every lane's copies are counted by the barrier before the expect-tx arrival below
+          // the tiled operand's TMA first; lane 0 arrives only after every lane's copies are
+          // counted by the barrier
+          if (lane == 0) {
+            mbar_expect_tx(bar, STAGE_BYTES - (MODE == DW13 ? B_BYTES : A_BYTES));
+            issue_half_loads<MODE>(p, tc, kb, rank, a_s, b_s, bar, true);
+          }
           gather_token_half<MODE>(p, tc, kb, rank, a_s, b_s, bar, lane);
           __syncwarp();
-        }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar, gather ? STAGE_BYTES - (MODE == DW13 ? B_BYTES : A_BYTES) : STAGE_BYTES);
-          issue_half_loads<MODE>(p, tc, kb, rank, a_s, b_s, bar, gather);
+          if (lane == 0) mbar_arrive(bar);
+        } else if (lane == 0) {
+          mbar_arrive_expect_tx(bar, STAGE_BYTES);
+          issue_half_loads<MODE>(p, tc, kb, rank, a_s, b_s, bar, false);
         }
         pending |= 1u << stage;
         pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
