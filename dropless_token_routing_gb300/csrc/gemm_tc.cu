@@ -112,14 +112,15 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
     tma2d(b_s, &p.b0, bar, kk, tc.ni * BN);
   } else if (MODE == FWD1) {
     const int j0 = tc.ni * (BN / 2);
+    // the weight rows first: for a light expert they stream from HBM and land last
     if (!G.shared) {
-      if (!gather) tma2d(a_s, &p.a0, bar, k0, row0 + m0);
       tma3d(b_s, &p.b0, bar, k0, j0, G.e);
       tma3d(b_s + B_BYTES / 2, &p.b0, bar, k0, a.f + j0, G.e);
+      if (!gather) tma2d(a_s, &p.a0, bar, k0, row0 + m0);
     } else {
-      tma2d(a_s, &p.a1, bar, k0, m0);
       tma3d(b_s, &p.b1, bar, k0, j0, G.s);
       tma3d(b_s + B_BYTES / 2, &p.b1, bar, k0, a.f_s + j0, G.s);
+      tma2d(a_s, &p.a1, bar, k0, m0);
     }
   } else if (MODE == FWD2) {
     const int n0 = tc.ni * BN;
