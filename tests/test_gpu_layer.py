@@ -217,6 +217,15 @@ def test_layer_step_replays_from_a_cuda_graph():
         assert torch.equal(layer.grads[k_], v), k_
 
 
+@pytest.mark.parametrize("k", [3, 8])
+def test_combine_rows_longer_than_one_segment(k):
+    """The combine's k <= 8 path hands each warp a segment of 1024 elements of one token's row:
+    d = 1088 gives every row a full segment and a ragged one of 64 elements, in the forward
+    combine and in the dX un-rearrangement."""
+    from layer_check import check_layer
+    check_layer(make_workload(shrink("pangu_bf16", T=100, d=1088, E=8, k=k, f=128, f_s=128)), bwd=True)
+
+
 # ---------------------------------------------------------------- randomised shapes
 def _random_shapes(n, seed):
     import random
