@@ -89,6 +89,13 @@ def algorithmic_work(cfg):
     return flops, bytes_
 
 
+def executed_rows(c):
+    """Rows the token-row products multiply for a group of c rows: 128-row M tiles, the last
+    one a 64-row tile when at most 64 rows are left."""
+    q, r = divmod(int(c), 128)
+    return q * 128 + (0 if r == 0 else 64 if r <= 64 else 128)
+
+
 def group_roofline(cfg, counts, peaks):
     """Per-group roofline of each grouped product: the sum over groups (the routed experts
     with their n_e token copies, then the shared experts over all T tokens) of
@@ -386,6 +393,7 @@ def summarize(cfg, trace, steps, counts, peaks):
     T = cfg["T"]
     rows = sum(counts) + cfg["S"] * T
     padded = sum(-(-c // 128) * 128 for c in counts) + cfg["S"] * (-(-T // 128) * 128)
+    executed = sum(executed_rows(c) for c in counts) + cfg["S"] * executed_rows(T)
     return {
         "kernels": kernels, "dominant": dom, "launches": sum(v[0] for v in trace.values()),
         "grouped_gemm": {"tflops": round(tf, 1),
@@ -395,7 +403,8 @@ def summarize(cfg, trace, steps, counts, peaks):
                          "per_group_roofline_ms": round(groof_ms, 3),
                          "frac_of_per_group_roofline": round(groof_ms / gemm_ms, 3) if gemm_ms else None},
         "routing": {"max_expert_rows": max(counts), "empty_experts": sum(1 for c in counts if c == 0),
-                    "m_tile_fill": round(rows / padded, 4)}}
+                    "m_tile_fill": round(rows / executed, 4) if executed else None,
+                    "m_tile_fill_128": round(rows / padded, 4) if padded else None}}
 
 
 def other_workload(name, args, dev, peaks, steps=10):

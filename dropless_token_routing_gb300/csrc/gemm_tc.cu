@@ -10,7 +10,8 @@
 // is rebuilt by every CTA from the device-resident expert offsets, so nothing waits on the
 // host. Tiles of one expert run N-tile major / M-tile minor so concurrently running CTAs
 // share the expert's weight tile through L2.
-// Ragged edges: M tails read neighbouring rows (or the TMA zero fill) and are not stored.
+// Ragged edges: M tails read neighbouring rows (or the TMA zero fill) and are not stored; a
+// group's last M tile with at most 64 rows runs as an M=64 MMA on a 64-row A box.
 // Every mbarrier wait is bounded (1 s); on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT,
 // drains its TMA loads and MMAs, frees its TMEM and exits.
 #include <cuda.h>
@@ -37,8 +38,19 @@ using namespace tc;
 
 struct TcParams {
   CUtensorMap a0, a1, b0, b1;
+  CUtensorMap h0, h1;   // A (routed / shared) in boxes of 64 rows, for the short last M tiles
   GroupedArgs g;
 };
+
+// A group's last M tile with at most 64 rows is multiplied as an M = 64 MMA on a 64-row A
+// box (rows 0..63 of the tile sit in TMEM lanes 32 q + 0..15, q = row / 16), so that the
+// ragged end of a segment does not pay for 128 rows. Gathered A tiles keep M = 128.
+template <int MODE>
+__device__ __forceinline__ bool short_tile(const GroupedArgs& a, const TileCoord& tc) {
+  if (MODE == ROUTER) return false;
+  if ((MODE == FWD1 || MODE == BWD2T) && a.gather_rows != nullptr && !tc.G.shared) return false;
+  return tc.G.M - tc.mi * BM <= BM / 2;
+}
 
 // ------------------------------------------------------------------ tcgen05 (one CTA)
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t idesc,
@@ -94,6 +106,30 @@ template <int MODE> struct ModeTraits {
   static constexpr int bn_eff = (MODE == FWD1) ? BN / 2 : BN;
 };
 
+// The MMAs of one tile's K blocks (instruction descriptor IDESC), each after its stage has
+// landed; the stage is released by a commit once they have read it. Returns false when a wait
+// ran out.
+template <int MODE, uint32_t IDESC>
+__device__ __forceinline__ bool mma_kloop(uint32_t smem_base, uint32_t d_tmem, int nkb, int& stage,
+                                          uint32_t& phase, uint64_t* full_bar, uint64_t* empty_bar,
+                                          volatile int* abort_flag, int* err, bool gathered) {
+  for (int kb = 0; kb < nkb; ++kb) {
+    if (!mbar_wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, err, kWaitLimitNs)) return false;
+    if (gathered) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_after();
+    const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < BK / 16; ++kk) {
+      const uint64_t ad = sdesc(a_s + kk * 32, 16, 1024);
+      const uint64_t bd = ModeTraits<MODE>::b_mn ? sdesc(b_s + kk * 2048, SLAB, 1024) : sdesc(b_s + kk * 32, 16, 1024);
+      umma(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+    }
+    umma_commit(smem_u32(&empty_bar[stage]));
+    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------ producer: TMA issue
 // `gather`: the routed A tile is gathered row by row by the whole producer warp instead
 // (gather_a_tile), so it is skipped here.
@@ -106,6 +142,9 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
   const int k0 = kb * BK;
   const int row0 = (int)G.row0;
   const int T = (int)a.T;
+  const bool sh_t = short_tile<MODE>(a, tc);
+  const CUtensorMap* am0 = sh_t ? &p.h0 : &p.a0;
+  const CUtensorMap* am1 = sh_t ? &p.h1 : &p.a1;
   if (MODE == ROUTER) {
     const int kk = G.k0 + k0;                 // K slice of this group
     tma2d(a_s, &p.a0, bar, kk % a.d, m0);     // x, read once per weight part
@@ -116,42 +155,42 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
     if (!G.shared) {
       tma3d(b_s, &p.b0, bar, k0, j0, G.e);
       tma3d(b_s + B_BYTES / 2, &p.b0, bar, k0, a.f + j0, G.e);
-      if (!gather) tma2d(a_s, &p.a0, bar, k0, row0 + m0);
+      if (!gather) tma2d(a_s, am0, bar, k0, row0 + m0);
     } else {
       tma3d(b_s, &p.b1, bar, k0, j0, G.s);
       tma3d(b_s + B_BYTES / 2, &p.b1, bar, k0, a.f_s + j0, G.s);
-      tma2d(a_s, &p.a1, bar, k0, m0);
+      tma2d(a_s, am1, bar, k0, m0);
     }
   } else if (MODE == FWD2) {
     const int n0 = tc.ni * BN;
     if (!G.shared) {
-      tma2d(a_s, &p.a0, bar, k0, row0 + m0);
+      tma2d(a_s, am0, bar, k0, row0 + m0);
       tma3d(b_s, &p.b0, bar, k0, n0, G.e);
     } else {
       const int kpb = a.f_s / BK, s = kb / kpb, kl = (kb - s * kpb) * BK;
-      tma2d(a_s, &p.a1, bar, kl, s * T + m0);
+      tma2d(a_s, am1, bar, kl, s * T + m0);
       tma3d(b_s, &p.b1, bar, kl, n0, s);
     }
   } else if (MODE == BWD2T) {
     const int n0 = tc.ni * BN;
     if (!G.shared) {
-      if (!gather) tma2d(a_s, &p.a0, bar, k0, row0 + m0);
+      if (!gather) tma2d(a_s, am0, bar, k0, row0 + m0);
 #pragma unroll
       for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b0, bar, n0 + 64 * i, k0, G.e);
     } else {
-      tma2d(a_s, &p.a1, bar, k0, m0);
+      tma2d(a_s, am1, bar, k0, m0);
 #pragma unroll
       for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b1, bar, n0 + 64 * i, k0, G.s);
     }
   } else if (MODE == BWD1T) {
     const int n0 = tc.ni * BN;
     if (!G.shared) {
-      tma2d(a_s, &p.a0, bar, k0, row0 + m0);
+      tma2d(a_s, am0, bar, k0, row0 + m0);
 #pragma unroll
       for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b0, bar, n0 + 64 * i, k0, G.e);
     } else {
       const int kpb = 2 * a.f_s / BK, s = kb / kpb, kl = (kb - s * kpb) * BK;
-      tma2d(a_s, &p.a1, bar, kl, s * T + m0);
+      tma2d(a_s, am1, bar, kl, s * T + m0);
 #pragma unroll
       for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b1, bar, n0 + 64 * i, kl, s);
     }
@@ -449,7 +488,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
           __syncwarp();
           if (lane == 0) mbar_arrive(bar);
         } else if (lane == 0) {
-          mbar_arrive_expect_tx(bar, STAGE_BYTES);
+          mbar_arrive_expect_tx(bar, short_tile<MODE>(a, tc) ? STAGE_BYTES - A_BYTES / 2 : STAGE_BYTES);
           issue_tile_loads<MODE>(p, tc, kb, a_s, b_s, bar, false);
         }
         pending |= 1u << stage;
@@ -480,22 +519,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
                                kWaitLimitNs)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full_bar[stage]), phase, &abort_flag, a.err,
-                                 kWaitLimitNs)) { ok = false; break; }
-          if (gathered) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          tc_fence_after();
-          const uint32_t a_s = smem_base + stage * STAGE_BYTES, b_s = a_s + A_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = sdesc(a_s + kk * 32, 16, 1024);
-            const uint64_t bd = TR::b_mn ? sdesc(b_s + kk * 2048, SLAB, 1024) : sdesc(b_s + kk * 32, 16, 1024);
-            umma(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-          }
-          issued = true;
-          umma_commit(smem_u32(&empty_bar[stage]));
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
+        if (nkb > 0) issued = true;
+        ok = short_tile<MODE>(a, tc)
+                 ? mma_kloop<MODE, idesc_bf16(BM / 2, BN, false, TR::b_mn)>(smem_base, d_tmem, nkb, stage, phase,
+                                                                            full_bar, empty_bar, &abort_flag, a.err,
+                                                                            gathered)
+                 : mma_kloop<MODE, idesc>(smem_base, d_tmem, nkb, stage, phase, full_bar, empty_bar, &abort_flag,
+                                          a.err, gathered);
         if (!ok) break;
         if (nkb > 0) umma_commit(smem_u32(&tfull_bar[b]));
         else mbar_arrive(smem_u32(&tfull_bar[b]));
@@ -520,7 +550,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
       if (!__all_sync(0xffffffffu, got)) break;   // warp-uniform: tcgen05.ld is .sync.aligned
       tc_fence_after();
       const uint32_t acc = tmem_base + ((uint32_t)(lg * 32) << 16) + (uint32_t)(b * BN);
-      epilogue_tile<MODE>(p, tc, r, acc, stage, lane);
+      // a short tile's rows 16 lg .. 16 lg + 15 are in lanes 0..15 of this warp's quarter; the
+      // other lanes get a row past the tile's end (not stored)
+      const int rr = short_tile<MODE>(a, tc) ? (lane < 16 ? lg * 16 + lane : BM / 2 + lane) : r;
+      epilogue_tile<MODE>(p, tc, rr, acc, stage, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[b]));
@@ -572,25 +605,30 @@ int launch_tc_grouped(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
   const bool sh = g.S > 0;
   switch (mode) {
     case FWD1:
-      ok = (g.gather_rows != nullptr || map2d(&p.a0, g.x_perm, d, Tk, 64, 128)) &&
+      ok = (g.gather_rows != nullptr || (map2d(&p.a0, g.x_perm, d, Tk, 64, 128) && map2d(&p.h0, g.x_perm, d, Tk, 64, 64))) &&
            map3d(&p.b0, g.w13, d, 2 * f, E, 64, 128);
-      if (sh) ok = ok && map2d(&p.a1, g.x, d, T, 64, 128) && map3d(&p.b1, g.ws13, d, 2 * fs, S, 64, 128);
+      if (sh) ok = ok && map2d(&p.a1, g.x, d, T, 64, 128) && map2d(&p.h1, g.x, d, T, 64, 64) &&
+                   map3d(&p.b1, g.ws13, d, 2 * fs, S, 64, 128);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<FWD1>(p, num_sms, st);
     case FWD2:
-      ok = map2d(&p.a0, g.h, f, Tk, 64, 128) && map3d(&p.b0, g.w2, f, d, E, 64, 256);
-      if (sh) ok = ok && map2d(&p.a1, g.h_sh, fs, ST, 64, 128) && map3d(&p.b1, g.ws2, fs, d, S, 64, 256);
+      ok = map2d(&p.a0, g.h, f, Tk, 64, 128) && map2d(&p.h0, g.h, f, Tk, 64, 64) && map3d(&p.b0, g.w2, f, d, E, 64, 256);
+      if (sh) ok = ok && map2d(&p.a1, g.h_sh, fs, ST, 64, 128) && map2d(&p.h1, g.h_sh, fs, ST, 64, 64) &&
+                   map3d(&p.b1, g.ws2, fs, d, S, 64, 256);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<FWD2>(p, num_sms, st);
     case BWD2T:
-      ok = (g.gather_rows != nullptr || map2d(&p.a0, g.dy_perm, d, Tk, 64, 128)) &&
+      ok = (g.gather_rows != nullptr || (map2d(&p.a0, g.dy_perm, d, Tk, 64, 128) && map2d(&p.h0, g.dy_perm, d, Tk, 64, 64))) &&
            map3d(&p.b0, g.w2, f, d, E, 64, 64);
-      if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 128) && map3d(&p.b1, g.ws2, fs, d, S, 64, 64);
+      if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 128) && map2d(&p.h1, g.dy, d, T, 64, 64) &&
+                   map3d(&p.b1, g.ws2, fs, d, S, 64, 64);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<BWD2T>(p, num_sms, st);
     case BWD1T:
-      ok = map2d(&p.a0, g.dz, 2 * f, Tk, 64, 128) && map3d(&p.b0, g.w13, d, 2 * f, E, 64, 64);
-      if (sh) ok = ok && map2d(&p.a1, g.dz_sh, 2 * fs, ST, 64, 128) && map3d(&p.b1, g.ws13, d, 2 * fs, S, 64, 64);
+      ok = map2d(&p.a0, g.dz, 2 * f, Tk, 64, 128) && map2d(&p.h0, g.dz, 2 * f, Tk, 64, 64) &&
+           map3d(&p.b0, g.w13, d, 2 * f, E, 64, 64);
+      if (sh) ok = ok && map2d(&p.a1, g.dz_sh, 2 * fs, ST, 64, 128) && map2d(&p.h1, g.dz_sh, 2 * fs, ST, 64, 64) &&
+                   map3d(&p.b1, g.ws13, d, 2 * fs, S, 64, 64);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<BWD1T>(p, num_sms, st);
     case ROUTER:

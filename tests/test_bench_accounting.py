@@ -99,5 +99,7 @@ def test_summarize_grouped_totals_and_dominant():
     assert r["grouped_gemm"]["tflops"] == pytest.approx(tf, abs=0.06)
     assert r["grouped_gemm"]["frac_of_burst_peak"] == pytest.approx(tf / 100.0, abs=1e-3)
     assert r["kernels"]["combine"]["unit"] == "GB/s"
-    # 128-row M tiles: (100 + 28 + 64 rows) in 128 + 128 + 128 slots
-    assert r["routing"]["m_tile_fill"] == pytest.approx(192 / 384, abs=1e-4)
+    # executed rows: 100 in a 128-row tile, 28 and 64 in 64-row tiles; all in 128-row tiles: 384
+    assert r["routing"]["m_tile_fill"] == pytest.approx(192 / 256, abs=1e-4)
+    assert r["routing"]["m_tile_fill_128"] == pytest.approx(192 / 384, abs=1e-4)
+    assert [bench.executed_rows(c) for c in (0, 1, 64, 65, 128, 129, 192, 193)] == [0, 64, 64, 128, 128, 192, 192, 256]
