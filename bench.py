@@ -608,14 +608,16 @@ def main():
 
     # ---------------------------------------------------------------- end to end
     # Every step copies its inputs from pinned host memory and reads y and dx back. The copies
-    # run on a second stream, double-buffered: step i+2's inputs land while step i computes,
-    # y is read back during the backward and dx during the next forward.
+    # run on two more streams (host-to-device and device-to-host, so the two directions
+    # overlap), double-buffered: step i+2's inputs land while step i computes, y is read back
+    # during the backward and dx during the next forward.
     h_x = x.cpu().pin_memory()
     h_dy = dy.cpu().pin_memory()
     h_li = li.cpu().pin_memory() if li is not None else None
     h_y = torch.empty_like(h_x).pin_memory()
     h_dx = torch.empty_like(h_x).pin_memory()
-    copy = torch.cuda.Stream(device=dev)
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
     d_in = [(torch.empty_like(x), torch.empty_like(dy), torch.empty_like(li) if li is not None else None)
             for _ in range(2)]
     ev_in = [torch.cuda.Event() for _ in range(2)]     # the slot's inputs have landed
@@ -623,17 +625,18 @@ def main():
     ev_y, ev_yd, ev_dx, ev_dxd = (torch.cuda.Event() for _ in range(4))
 
     def h2d(slot):
-        with torch.cuda.stream(copy):
-            copy.wait_event(ev_used[slot])
+        with torch.cuda.stream(up):
+            up.wait_event(ev_used[slot])
             bx, bdy, bli = d_in[slot]
             bx.copy_(h_x, non_blocking=True)
             bdy.copy_(h_dy, non_blocking=True)
             if bli is not None:
                 bli.copy_(h_li, non_blocking=True)
-            ev_in[slot].record(copy)
+            ev_in[slot].record(up)
 
     def e2e_run(n):
-        copy.wait_stream(stream)
+        up.wait_stream(stream)
+        down.wait_stream(stream)
         for s_ in range(min(2, n)):
             h2d(s_)
         for i in range(n):
@@ -643,28 +646,29 @@ def main():
             stream.wait_event(ev_yd)          # the previous y has been read back
             y = layer.forward(bx, bli)
             ev_y.record(stream)
-            with torch.cuda.stream(copy):
-                copy.wait_event(ev_y)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_y)
                 h_y.copy_(y, non_blocking=True)
-                ev_yd.record(copy)
+                ev_yd.record(down)
             stream.wait_event(ev_dxd)         # the previous dx has been read back
             g = layer.backward(bdy)
             ev_used[s_].record(stream)
             ev_dx.record(stream)
-            with torch.cuda.stream(copy):
-                copy.wait_event(ev_dx)
+            with torch.cuda.stream(down):
+                down.wait_event(ev_dx)
                 h_dx.copy_(g["dx"], non_blocking=True)
-                ev_dxd.record(copy)
+                ev_dxd.record(down)
             if i + 2 < n:
                 h2d(s_)                       # the inputs of step i + 2
-        stream.wait_stream(copy)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
 
     e2e_run(2)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k_e2e = max(3, args.steps // 2)
+    k_e2e = max(3, args.steps)
     e2.record(stream)
     e2e_run(k_e2e)
     e3.record(stream)
