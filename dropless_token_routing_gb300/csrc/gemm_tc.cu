@@ -33,6 +33,10 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_STAGE_BYTES + 1024;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int SLAB = 64 * 128;                // one 64-element-wide, 64-row swizzled slab
+// A group of more than kPanelM M tiles is walked in panels of kPanelM M tiles (N-tile major
+// inside a panel), so that a heavy expert's token rows are re-read from L2 by its N tiles
+// rather than from HBM; a panel's weight tile is read once per panel.
+constexpr int kPanelM = 16;
 
 using namespace tc;
 
@@ -458,7 +462,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     uint32_t pend_par = 0;   // parity of the phase that load completes, per stage
     bool ok = true;
     for (TileCursor cur(sched, ng, blockIdx.x, gridDim.x); cur.valid() && ok; cur.advance()) {
-      const TileCoord tc = cur.coord(a, MODE, BM, s_off);
+      const TileCoord tc = cur.coord(a, MODE, BM, s_off, MODE == ROUTER ? 0 : kPanelM, TR::bn_eff);
       const int nkb = (tc.G.K + BK - 1) / BK;
       // fused rearrangement: lane L gathers chunk L % 8 of tile rows 4i + L / 8 (rows past the
       // segment repeat its first row; they are computed but never stored)
@@ -509,7 +513,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
       bool issued = false, ok = true;
       int it = 0;
       for (TileCursor cur(sched, ng, blockIdx.x, gridDim.x); cur.valid() && ok; cur.advance(), ++it) {
-        const TileCoord tc = cur.coord(a, MODE, BM, s_off);
+        const TileCoord tc = cur.coord(a, MODE, BM, s_off, MODE == ROUTER ? 0 : kPanelM, TR::bn_eff);
         const int nkb = (tc.G.K + BK - 1) / BK;
         const int b = it & 1;
         // a gathered A tile was written through the generic proxy (cp.async): order it before
@@ -543,7 +547,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_grouped_kernel(const __grid
     uint8_t* stage = smem + STAGES * STAGE_BYTES + (warp - 2) * EPI_STAGE_BYTES;
     int it = 0;
     for (TileCursor cur(sched, ng, blockIdx.x, gridDim.x); cur.valid(); cur.advance(), ++it) {
-      const TileCoord tc = cur.coord(a, MODE, BM, s_off);
+      const TileCoord tc = cur.coord(a, MODE, BM, s_off, MODE == ROUTER ? 0 : kPanelM, TR::bn_eff);
       const int b = it & 1;
       const bool got = mbar_wait_bounded(smem_u32(&tfull_bar[b]), (it >> 1) & 1, &abort_flag,
                                          a.err, kWaitLimitNs);

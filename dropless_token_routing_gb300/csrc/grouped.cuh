@@ -253,7 +253,10 @@ struct TileCursor {
     r += dr;
     if (r >= tot) { r -= tot; ++q; }
   }
-  __device__ __forceinline__ TileCoord coord(const GroupedArgs& a, int mode, int bm, const int* s_off) {
+  // panel > 0: a group of more than `panel` M tiles is walked in panels of `panel` M tiles,
+  // N-tile major inside each panel (bn = output columns of a tile along N)
+  __device__ __forceinline__ TileCoord coord(const GroupedArgs& a, int mode, int bm, const int* s_off,
+                                             int panel = 0, int bn = 256) {
     // tile is stream 0's iff floor((tile + 1) n0 / tot) > floor(tile n0 / tot)
     const bool s0 = r + n0 >= tot;
     const int j = s0 ? q : tile - q;
@@ -270,8 +273,17 @@ struct TileCursor {
     c.G = G;
     const int local = j - st[gg];
     const int mt = (G.M + bm - 1) / bm;
-    c.ni = local / mt;
-    c.mi = local - c.ni * mt;
+    if (panel <= 0 || mt <= panel) {
+      c.ni = local / mt;
+      c.mi = local - c.ni * mt;
+    } else {
+      const int nt = (G.N + bn - 1) / bn;
+      const int p = local / (panel * nt);
+      const int r0 = local - p * panel * nt;
+      const int pm = min(panel, mt - p * panel);   // M tiles of this panel
+      c.ni = r0 / pm;
+      c.mi = p * panel + (r0 - c.ni * pm);
+    }
     return c;
   }
 };
