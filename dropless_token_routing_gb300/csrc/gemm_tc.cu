@@ -169,7 +169,10 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
     const int n0 = tc.ni * BN;
     if (!G.shared) {
       tma2d(a_s, am0, bar, k0, row0 + m0);
-      tma3d(b_s, &p.b0, bar, k0, n0, G.e);
+      // an expert of one M tile reads its W2 rows once: they leave L2 first (measured 2 %
+      // faster here; the same policy on the MN-major weight slabs of BWD2T / BWD1T is slower)
+      if (G.M <= BM) tma3d_hint(b_s, &p.b0, bar, k0, n0, G.e, l2_evict_first());
+      else tma3d(b_s, &p.b0, bar, k0, n0, G.e);
     } else {
       const int kpb = a.f_s / BK, s = kb / kpb, kl = (kb - s * kpb) * BK;
       tma2d(a_s, am1, bar, kl, s * T + m0);
