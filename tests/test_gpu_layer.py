@@ -226,6 +226,14 @@ def test_combine_rows_longer_than_one_segment(k):
     check_layer(make_workload(shrink("pangu_bf16", T=100, d=1088, E=8, k=k, f=128, f_s=128)), bwd=True)
 
 
+def test_experts_larger_than_one_tile_panel():
+    """Groups of more than 16 M tiles (2048 rows) are walked in panels of 16 M tiles, the last
+    one short (here 2 and 3 M tiles, the shared expert's last one a 64-row tile): T = 2200
+    tokens on two experts and a shared expert, against the oracle."""
+    from layer_check import check_layer
+    check_layer(make_workload(shrink("pangu_bf16", T=2200, d=256, E=2, k=2, f=256, f_s=256)), bwd=True)
+
+
 # ---------------------------------------------------------------- randomised shapes
 def _random_shapes(n, seed):
     import random
