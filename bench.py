@@ -40,12 +40,12 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the small case T=1024, E=32
     # (33 gradient groups, 9216 token-copy rows), one launch after warm-up, scaled to the full
     # workload by the units each term grows with: reads by the token-copy rows (73728 / 9216),
-    # writes by the gradient groups (257 / 33). Small case: 217.3 MB read, 2016.8 MB
-    # written; scaled: 1738.1 MB + 15706.4 MB. See profiles/gemm_dw13_pangu_bf16.md.
+    # writes by the gradient groups (257 / 33). Small case: 217.3 MB read, 2016.4 MB
+    # written; scaled: 1738.1 MB + 15703.7 MB. See profiles/gemm_dw13_pangu_bf16.md.
     # Applies only while the kernel's source file is unchanged since the capture.
     "gemm_dw13": {"src": "gemm_tc_pair.cu", "workload": "pangu_bf16",
-                  "bytes_per_launch": 1738119168 + 15706380614,
-                  "src_sha256": "ebe602d5efffe650047c60502e590f7caf250704f798b6ee5f00a6f3ca2f5095"},
+                  "bytes_per_launch": 1738121216 + 15703657224,
+                  "src_sha256": "c47d5ddf42610731276e0491f165b3f35a98cd86bb778b8b9ab1c4af3cf87f24"},
 }
 
 

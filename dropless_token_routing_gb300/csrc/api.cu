@@ -2,6 +2,8 @@
 // Nothing here synchronises with the device except moe_get_device_error.
 #include <string.h>
 
+#include <mutex>
+
 #include "grouped.cuh"
 #include "internal.h"
 
@@ -64,9 +66,12 @@ struct DevInfo {
 };
 
 DevInfo dev_info() {
-  static DevInfo cache[64];
+  // per device, filled once under a lock (callers may be several host threads)
+  static std::mutex mu;
+  static DevInfo cache[kMaxDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DevInfo();
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DevInfo();
+  std::lock_guard<std::mutex> lk(mu);
   if (cache[dev].sms == 0) {
     int sms = 0, ma = 0, mi = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

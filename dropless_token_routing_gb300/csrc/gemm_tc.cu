@@ -16,6 +16,8 @@
 // drains its TMA loads and MMAs, frees its TMEM and exits.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "grouped.cuh"
 #include "tc_common.cuh"
 #include "internal.h"
@@ -585,12 +587,20 @@ constexpr int trace_phase_of(int mode) {
 
 template <int MODE>
 int launch_mode(TcParams& p, int num_sms, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(tc_grouped_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set = true;
+  // the shared-memory attribute is set once per device (under a lock: callers may be several
+  // host threads, each with its own device)
+  static std::mutex mu;
+  static bool attr_set[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(tc_grouped_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      attr_set[dev] = true;
+    }
   }
   TraceScope ts(trace_phase_of(MODE), st);
   tc_grouped_kernel<MODE><<<num_sms, NUM_THREADS, SMEM_BYTES, st>>>(p);

@@ -30,6 +30,8 @@
 // CTAs meet at a cluster barrier before they release the tensor memory.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "grouped.cuh"
 #include "internal.h"
 #include "tc_common.cuh"
@@ -466,20 +468,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<EW>::THREADS
 template <int MODE, int EW>
 int launch_pair_ew(PairParams& p, int num_sms, cudaStream_t st) {
   constexpr int SMEM_BYTES = PairCfg<EW>::SMEM_BYTES, THREADS = PairCfg<EW>::THREADS;
-  static int occ = 0;  // pairs that can be resident at once
-  if (occ == 0) {
-    if (cudaFuncSetAttribute(tc_pair_dw_kernel<MODE, EW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3((unsigned)(num_sms & ~1));
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_pair_dw_kernel<MODE, EW>, &cfg) != cudaSuccess || n <= 0)
-      return MOE_ERR_CUDA;
-    occ = n;
+  // per device, once (under a lock: callers may be several host threads): the shared-memory
+  // attribute and the pairs that can be resident at once
+  static std::mutex mu;
+  static int occ_dev[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  int occ;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (occ_dev[dev] == 0) {
+      if (cudaFuncSetAttribute(tc_pair_dw_kernel<MODE, EW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      cudaLaunchConfig_t cfg;
+      memset(&cfg, 0, sizeof(cfg));
+      cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+      cfg.blockDim = dim3(THREADS);
+      cfg.dynamicSmemBytes = SMEM_BYTES;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, tc_pair_dw_kernel<MODE, EW>, &cfg) != cudaSuccess || n <= 0)
+        return MOE_ERR_CUDA;
+      occ_dev[dev] = n;
+    }
+    occ = occ_dev[dev];
   }
   const int nc = occ < num_sms / 2 ? occ : num_sms / 2;
   TraceScope ts(MODE == DW13 ? TP_GEMM_DW13 : TP_GEMM_DW2, st);

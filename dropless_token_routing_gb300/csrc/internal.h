@@ -16,6 +16,7 @@ constexpr int kDwrSplit = 8;      // fixed row split of the router dW reduction
 constexpr int kMaxShared = 8;     // shared experts supported
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;
+constexpr int kMaxDevices = 64;   // device ordinals the per-device host caches cover
 
 inline size_t elt_bytes(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 

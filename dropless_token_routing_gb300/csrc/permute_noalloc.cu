@@ -29,7 +29,6 @@ constexpr int64_t kNoAllocScratchInts = 2 * kNoAllocMaxChunkCells + kNoAllocMaxC
 // [chunk histograms | chunk bases | local ranks], int32
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchInts];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices];
 
