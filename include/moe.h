@@ -24,6 +24,9 @@
  *  - Tensor pointers are DEVICE pointers owned by the caller, row-major, 16-byte aligned.
  *    The library allocates and frees nothing.
  *  - Calls are asynchronous on `stream` and never synchronise (except moe_get_device_error).
+ *  - Calls run on the calling thread's current CUDA device. Several host threads may call the
+ *    library at once (each with its own device, or its own stream and workspace): the one-time
+ *    per-device setup (kernel attributes, device properties) is made under a lock.
  *  - Activations and expert weights are fp32 (MOE_F32) or bf16 (MOE_BF16) as dims->dtype says;
  *    router weights, scores, gates, dgate and score gradients are always fp32; indices int32.
  *  - Expert weights are K-major: W13 [E][2f][d] (gate rows 0..f-1, up rows f..2f-1),
