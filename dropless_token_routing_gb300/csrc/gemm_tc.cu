@@ -8,8 +8,8 @@
 //   warps 2..5  epilogue: tcgen05.ld -> fused math of the mode -> bf16 -> global memory
 // The tile schedule (groups = routed experts with ragged row counts, then shared experts)
 // is rebuilt by every CTA from the device-resident expert offsets, so nothing waits on the
-// host. Tiles of one expert run N-tile major / M-tile minor so concurrently running CTAs
-// share the expert's weight tile through L2.
+// host. Tiles of one expert run N-tile major / M-tile minor (a heavy expert in panels of 16
+// M tiles) so concurrently running CTAs share the expert's weight tile through L2.
 // Ragged edges: M tails read neighbouring rows (or the TMA zero fill) and are not stored; a
 // group's last M tile with at most 64 rows runs as an M=64 MMA on a 64-row A box.
 // Every mbarrier wait is bounded (1 s); on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT,

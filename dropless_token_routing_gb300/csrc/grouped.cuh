@@ -219,8 +219,8 @@ struct TileCoord {
 // The two streams are merged in proportion: of the first i tiles, floor(i * n0 / (n0 + n1))
 // come from stream 0, so every stretch of the launch holds both kinds of tile. Within a
 // stream the groups keep their order, and the tiles of a group are ordered N-tile major,
-// M-tile minor, so that CTAs working at the same time on one expert share its weight tile
-// through L2. Each step costs a few integer operations: the merge position is carried as a
+// M-tile minor (optionally in panels of M tiles, see coord), so that CTAs working at the
+// same time on one expert share its weight tile through L2. Each step costs a few integer operations: the merge position is carried as a
 // quotient and remainder, and the group of each stream only moves forward. (The issuing
 // threads of the short-K dW tiles cannot afford a search or a 64-bit division per tile.)
 struct TileCursor {
