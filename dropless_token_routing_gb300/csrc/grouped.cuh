@@ -253,8 +253,8 @@ struct TileCursor {
     r += dr;
     if (r >= tot) { r -= tot; ++q; }
   }
-  // panel > 0: a group of more than `panel` M tiles is walked in panels of `panel` M tiles,
-  // N-tile major inside each panel (bn = output columns of a tile along N)
+  // panel > 0: a group of more than `panel` M tiles and K of at least 4096 is walked in panels
+  // of `panel` M tiles, N-tile major inside each panel (bn = output columns of a tile along N)
   __device__ __forceinline__ TileCoord coord(const GroupedArgs& a, int mode, int bm, const int* s_off,
                                              int panel = 0, int bn = 256) {
     // tile is stream 0's iff floor((tile + 1) n0 / tot) > floor(tile n0 / tot)
@@ -273,7 +273,8 @@ struct TileCursor {
     c.G = G;
     const int local = j - st[gg];
     const int mt = (G.M + bm - 1) / bm;
-    if (panel <= 0 || mt <= panel) {
+    // (a K below 4096 keeps a 128-row block of A under 1 MB: it stays in L2 without panels)
+    if (panel <= 0 || mt <= panel || G.K < 4096) {
       c.ni = local / mt;
       c.mi = local - c.ni * mt;
     } else {
