@@ -234,6 +234,61 @@ def test_experts_larger_than_one_tile_panel():
     check_layer(make_workload(shrink("pangu_bf16", T=2200, d=256, E=2, k=2, f=256, f_s=256)), bwd=True)
 
 
+_THREADS_SCRIPT = r"""
+import sys, threading
+import torch
+sys.path.insert(0, sys.argv[1])
+from synth import make_workload, shrink
+from dropless_token_routing_gb300.api import LayerParams, MoELayer
+
+cfg = shrink("pangu_bf16", T=300, d=256, E=8, k=2, f=128, f_s=128)
+ws = [make_workload(cfg, device="cuda", replica=r) for r in (0, 1)]
+def build(w):
+    p = LayerParams(w13=w.w13, w2=w.w2, w_r=w.w_r, bias=w.bias, ws13=w.ws13, ws2=w.ws2)
+    c = w.cfg
+    lay = MoELayer(p, c["T"], c["d"], c["E"], c["k"], c["f"], c["S"], c["f_s"], torch.bfloat16)
+    lay.alloc_grads()
+    return lay
+layers = [build(w) for w in ws]
+torch.cuda.synchronize()
+out = [None, None]
+gate = threading.Barrier(2)
+def run(i):
+    s = torch.cuda.Stream()
+    gate.wait()   # both threads make their first library calls (one-time setup) at once
+    for _ in range(3):
+        y = layers[i].forward(ws[i].x, stream=s)
+        g = layers[i].backward(ws[i].dy, stream=s)
+    s.synchronize()
+    out[i] = (y.clone(), {k: v.clone() for k, v in g.items() if v is not None})
+th = [threading.Thread(target=run, args=(i,)) for i in (0, 1)]
+for t in th: t.start()
+for t in th: t.join()
+for i in (0, 1):   # the same layers again, one after the other
+    y = layers[i].forward(ws[i].x)
+    g = layers[i].backward(ws[i].dy)
+    torch.cuda.synchronize()
+    assert torch.equal(y, out[i][0]), i
+    for k, v in out[i][1].items():
+        assert torch.equal(g[k], v), (i, k)
+assert not torch.equal(out[0][0], out[1][0])
+print("ok")
+"""
+
+
+def test_two_host_threads_call_the_library_at_once():
+    """Two host threads, each with its own layer, workspace and stream, make their first calls
+    into a freshly loaded library at the same moment (the per-device one-time setup runs under
+    a lock) and run three steps; each thread's results equal the same layer run alone."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _THREADS_SCRIPT, root], capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stderr[-2000:]
+
+
 # ---------------------------------------------------------------- randomised shapes
 def _random_shapes(n, seed):
     import random
