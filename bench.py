@@ -40,12 +40,12 @@ NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on the small case T=1024, E=32
     # (33 gradient groups, 9216 token-copy rows), one launch after warm-up, scaled to the full
     # workload by the units each term grows with: reads by the token-copy rows (73728 / 9216),
-    # writes by the gradient groups (257 / 33). Small case: 217.3 MB read, 2016.4 MB
-    # written; scaled: 1738.1 MB + 15703.7 MB. See profiles/gemm_dw13_pangu_bf16.md.
+    # writes by the gradient groups (257 / 33). Small case: 217.6 MB read, 2018.9 MB
+    # written; scaled: 1741.0 MB + 15723.2 MB. See profiles/gemm_dw13_pangu_bf16.md.
     # Applies only while the kernel's source file is unchanged since the capture.
     "gemm_dw13": {"src": "gemm_tc_pair.cu", "workload": "pangu_bf16",
-                  "bytes_per_launch": 1738121216 + 15703657224,
-                  "src_sha256": "c47d5ddf42610731276e0491f165b3f35a98cd86bb778b8b9ab1c4af3cf87f24"},
+                  "bytes_per_launch": 1741023232 + 15723167542,
+                  "src_sha256": "d4145c7d9898e288cc3eb2b62baa12a1b453960ea9c48e6a6abb6d93bee45e33"},
 }
 
 
