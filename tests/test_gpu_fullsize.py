@@ -311,3 +311,30 @@ def test_capacity_fullsize_permutation_and_sampled_tokens(run_capacity):
     assert _rel(_f64(layer.y[toks]), y_ref) <= TOL
     assert _rel(_f64(g["dx"][toks]), dx_ref) <= TOL
     assert _rel(_f64(g["dlogits"][toks]), dscores) <= TOL
+
+
+def test_fused_gather_at_full_size_matches_the_copies_bitwise():
+    """The Pangu-shaped layer at its full size with the rearrangement fused into the GEMMs'
+    operand loads (row gathers from x and dY) gives the copy path's outputs and gradients bit
+    for bit: the gathered rows are the same bf16 values, fed in the same order."""
+    from dropless_token_routing_gb300.api import LayerParams, MoELayer, get_device_error
+    cfg = dict(CONFIGS["pangu_bf16"], name="pangu_bf16")
+    w = make_workload(cfg, device="cuda")
+    params = LayerParams(w13=w.w13, w2=w.w2, w_r=w.w_r, bias=w.bias, ws13=w.ws13, ws2=w.ws2)
+    out = []
+    for rearrange in (0, 1):
+        layer = MoELayer(params, cfg["T"], cfg["d"], cfg["E"], cfg["k"], cfg["f"], cfg["S"], cfg["f_s"],
+                         torch.bfloat16, rearrange=rearrange, recompute=bool(rearrange))
+        layer.alloc_grads()
+        y = layer.forward(w.x).clone()
+        g = layer.backward(w.dy)
+        torch.cuda.synchronize()
+        assert get_device_error(layer.ws) == 0
+        # both layers' gradients stay on the device (about 24 GB each) and are compared whole
+        out.append((y, {n: v for n, v in g.items() if v is not None}))
+        del layer
+    assert torch.equal(out[0][0], out[1][0])
+    for n in out[0][1]:
+        assert torch.equal(out[0][1][n], out[1][1][n]), n
+    del out
+    torch.cuda.empty_cache()
