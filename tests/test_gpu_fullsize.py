@@ -313,18 +313,20 @@ def test_capacity_fullsize_permutation_and_sampled_tokens(run_capacity):
     assert _rel(_f64(g["dlogits"][toks]), dscores) <= TOL
 
 
-def test_fused_gather_at_full_size_matches_the_copies_bitwise():
+@pytest.mark.parametrize("rearrange,recompute", [(1, True), (0, True)])
+def test_fused_gather_at_full_size_matches_the_copies_bitwise(rearrange, recompute):
     """The Pangu-shaped layer at its full size with the rearrangement fused into the GEMMs'
-    operand loads (row gathers from x and dY) gives the copy path's outputs and gradients bit
-    for bit: the gathered rows are the same bf16 values, fed in the same order."""
+    operand loads (row gathers from x and dY), or with selective recompute alone (x_perm and h
+    not kept), gives the plain path's outputs and gradients bit for bit: the gathered or
+    recomputed rows are the same bf16 values, fed in the same order."""
     from dropless_token_routing_gb300.api import LayerParams, MoELayer, get_device_error
     cfg = dict(CONFIGS["pangu_bf16"], name="pangu_bf16")
     w = make_workload(cfg, device="cuda")
     params = LayerParams(w13=w.w13, w2=w.w2, w_r=w.w_r, bias=w.bias, ws13=w.ws13, ws2=w.ws2)
     out = []
-    for rearrange in (0, 1):
+    for re_, rc_ in ((0, False), (rearrange, recompute)):
         layer = MoELayer(params, cfg["T"], cfg["d"], cfg["E"], cfg["k"], cfg["f"], cfg["S"], cfg["f_s"],
-                         torch.bfloat16, rearrange=rearrange, recompute=bool(rearrange))
+                         torch.bfloat16, rearrange=re_, recompute=rc_)
         layer.alloc_grads()
         y = layer.forward(w.x).clone()
         g = layer.backward(w.dy)
