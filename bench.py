@@ -336,10 +336,16 @@ def drop_and_pad(factors, params, cfg, w, counts, args, stream):
 
 
 def fused_rearrange(params, cfg, w, args, stream):
-    """The rearrangement fused into the expert GEMMs' operand loads (TMA row gathers from x
-    and dy, no rearranged copies) instead of the copies the default step makes."""
-    ms = time_variant(params, cfg, w, args, stream, rearrange=1, recompute=True)
-    return {"value": round(cfg["T"] / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3)}
+    """The rearrangement fused into the expert GEMMs' operand loads (row gathers from x and
+    dy, no rearranged copies) instead of the copies the default step makes; and the
+    un-rearrangement fused into the second expert GEMM's stores (token-major rows, so the
+    combine reads each token's rows as one block), alone and with the gathers."""
+    out = {}
+    for key, r in (("gather", 1), ("scatter", 2), ("gather_and_scatter", 3)):
+        ms = time_variant(params, cfg, w, args, stream, rearrange=r, recompute=bool(r & 1))
+        out[key] = {"value": round(cfg["T"] / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 3)}
+    # the gather variant's figures stay at the top level, as before
+    return dict(out["gather"], variants=out)
 
 
 # --------------------------------------------------------------------------- summaries
@@ -477,9 +483,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shrink", default="", help="smaller case of the same recipe, e.g. T=512,E=16 "
                                                   "(for profiler captures; not a bench line)")
-    ap.add_argument("--rearrange", default="copy", choices=["copy", "gather"],
-                    help="the timed step's rearrangement: rearranged copies (default) or TMA row "
-                         "gathers fused into the expert GEMMs (with selective recompute)")
+    ap.add_argument("--rearrange", default="copy", choices=["copy", "gather", "scatter", "both"],
+                    help="the timed step's rearrangement: rearranged copies (default), row gathers "
+                         "fused into the expert GEMMs (with selective recompute), the second GEMM "
+                         "writing token-major rows for the combine, or both")
     ap.add_argument("--no-fused-rearrange", dest="fused_rearrange", action="store_false",
                     help="skip the timing of the fused-rearrangement variant (rank 0, after the "
                          "main measurement)")
@@ -555,14 +562,17 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     w = make_workload(cfg, device=dev, replica=rank)   # data parallel: each rank its own tokens
     params = LayerParams(w13=w.w13, w2=w.w2, w_r=w.w_r, bias=w.bias, ws13=w.ws13, ws2=w.ws2)
-    gather = args.rearrange == "gather"
+    rflag = {"copy": 0, "gather": 1, "scatter": 2, "both": 3}[args.rearrange]
+    gather = bool(rflag & 1)
     layer = MoELayer(params, T, cfg["d"], cfg["E"], cfg["k"], cfg["f"], cfg["S"], cfg["f_s"],
                      w.torch_dtype, device=dev, logits_input=w.logits_in is not None,
-                     rearrange=1 if gather else 0, recompute=gather)
+                     rearrange=rflag, recompute=gather)
     layer.alloc_grads()
     x, dy, li = w.x, w.dy, w.logits_in
-    if gather:
-        workload_cfg["rearrange"] = "TMA row gathers fused into the expert GEMMs"
+    if rflag:
+        workload_cfg["rearrange"] = {1: "row gathers fused into the expert GEMMs",
+                                     2: "token-major rows written by the second expert GEMM",
+                                     3: "row gathers and token-major rows fused into the GEMMs"}[rflag]
     stream = torch.cuda.current_stream()
 
     def step():

@@ -33,7 +33,8 @@ def _dt(dtype) -> int:
 
 def make_dims(T, d, E, k, f, S=0, f_s=0, dtype=torch.bfloat16, capacity=0, rearrange=0) -> N.MoeDims:
     """capacity = 0: dropless; C > 0: drop-and-pad with C rows per expert.
-    rearrange = 0: rearranged copies; 1: rearrangement fused into the GEMM loads."""
+    rearrange (flags) = 0: rearranged copies; 1: rearrangement fused into the GEMM loads;
+    2: the second expert GEMM writes its rows in token-major order for the combine; 3: both."""
     return N.MoeDims(int(T), int(d), int(E), int(k), int(f), int(S), int(f_s) if S else 0, _dt(dtype),
                      int(capacity), int(rearrange))
 
@@ -178,7 +179,8 @@ class MoELayer:
     moe_layer_bwd on the values the last forward saved. ``recompute=True`` keeps neither
     the rearranged input nor h between the two (selective recompute). ``capacity=C > 0``
     runs the drop-and-pad variant with C rows per expert instead of the dropless layer;
-    ``rearrange=1`` fuses the rearrangement into the GEMMs' operand loads.
+    ``rearrange=1`` fuses the rearrangement into the GEMMs' operand loads, ``rearrange=2`` the
+    un-rearrangement into the second GEMM's stores (token-major rows), 3 both.
     """
 
     def __init__(self, params: LayerParams, T, d, E, k, f, S=0, f_s=0, dtype=torch.bfloat16,

@@ -54,6 +54,7 @@ WsLayout ws_layout(const moe_dims& d) {
   L.dest_full = take(cap ? 4 * Tk : 0);
   L.row_src_full = take(cap ? 4 * Tk : 0);
   L.offsets_full = take(cap ? 4 * (E + 1) : 0);
+  L.scatter_rows = take(((d.rearrange & MOE_REARRANGE_SCATTER) && !cap) ? 4 * Tk : 0);
   L.total = o;
   return L;
 }
@@ -117,7 +118,7 @@ int check_dims(const moe_dims* d) {
   const int unit = d->dtype == MOE_BF16 ? 64 : 8;
   if (d->d % unit != 0 || d->f % unit != 0 || (d->S > 0 && d->f_s % unit != 0)) return MOE_ERR_BAD_DIMS;
   if (d->capacity < 0 || (int64_t)d->capacity * d->E >= (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
-  if (d->rearrange != MOE_REARRANGE_COPY && d->rearrange != MOE_REARRANGE_GATHER) return MOE_ERR_BAD_DIMS;
+  if (d->rearrange < 0 || d->rearrange > (MOE_REARRANGE_GATHER | MOE_REARRANGE_SCATTER)) return MOE_ERR_BAD_DIMS;
   const int64_t rows = d->T * (int64_t)d->k + perm_rows(*d) + (int64_t)d->S * d->T;
   if (d->T > (int64_t)0x7fffffff || rows >= (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
   return MOE_OK;
@@ -197,7 +198,14 @@ int run_router(const void* x, const float* w_r, const moe_dims* d, float* logits
 // so x_perm and dy_perm are never materialised. fp32 (SIMT kernels) and drop-and-pad (zero
 // padding rows) always keep the rearranged copies.
 bool fused_gather(const moe_dims* d) {
-  return d->rearrange == MOE_REARRANGE_GATHER && d->dtype == MOE_BF16 && d->capacity == 0;
+  return (d->rearrange & MOE_REARRANGE_GATHER) && d->dtype == MOE_BF16 && d->capacity == 0;
+}
+
+// MOE_REARRANGE_SCATTER on the bf16 dropless path: the layer forward's second expert GEMM
+// writes each output row at its token-major slot, and the combine reads each token's k rows
+// as one block (no dest gather).
+bool fused_scatter(const moe_dims* d) {
+  return (d->rearrange & MOE_REARRANGE_SCATTER) && d->dtype == MOE_BF16 && d->capacity == 0;
 }
 
 int dgate_tiles(const moe_dims* d) {
@@ -623,9 +631,15 @@ int moe_layer_fwd(const moe_layer_params* params, const void* x, const float* lo
   void* y_perm = w + L.y_perm;
   void* y_sh = dims->S > 0 ? (void*)(w + L.y_sh) : nullptr;
   a.h = h; a.h_sh = h_sh; a.y_perm = y_perm; a.y_sh = y_sh;
+  const bool scatter = fused_scatter(dims);
+  if (scatter) {   // y_perm then holds the expert outputs in token-major order
+    int32_t* srows = reinterpret_cast<int32_t*>(w + L.scatter_rows);
+    MOE_LAUNCH(launch_scatter_rows(saved->dest, dims->T * (int64_t)dims->k, srows, st));
+    a.scatter_rows = srows;
+  }
   MOE_TRY(run_grouped(FWD2, a, dims, st));
-  MOE_LAUNCH(launch_combine(y_perm, saved->dest, saved->topk_w, y_sh, nullptr, nullptr, nullptr,
-                            *dims, y, st));
+  MOE_LAUNCH(launch_combine(y_perm, scatter ? nullptr : saved->dest, saved->topk_w, y_sh, nullptr, nullptr,
+                            nullptr, *dims, y, st));
   return MOE_OK;
 }
 

@@ -381,9 +381,12 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const TileCoord
   } else {  // FWD2 / BWD1T: rows of ragged expert segments, stored row by row
     const int n0 = tc.ni * BN;
     __nv_bfloat16* out;
-    if (MODE == FWD2)
-      out = G.shared ? (__nv_bfloat16*)a.y_sh + (int64_t)m * a.d
-                     : (__nv_bfloat16*)a.y_perm + (G.row0 + m) * (int64_t)a.d;
+    if (MODE == FWD2) {
+      // the fused un-rearrangement writes a routed row at its token-major slot
+      const int64_t orow = G.row0 + m;
+      const int64_t srow = a.scatter_rows != nullptr && row_ok ? __ldg(a.scatter_rows + orow) : orow;
+      out = G.shared ? (__nv_bfloat16*)a.y_sh + (int64_t)m * a.d : (__nv_bfloat16*)a.y_perm + srow * a.d;
+    }
     else
       out = G.shared ? (__nv_bfloat16*)a.dx_sh + (int64_t)m * a.d
                      : (__nv_bfloat16*)a.dx_perm + (G.row0 + m) * (int64_t)a.d;

@@ -41,6 +41,9 @@ struct GroupedArgs {
   // permuted token rows are not read from x_perm / dy_perm but gathered from x / dy, row r
   // of the permuted order being token gather_rows[r] (the permutation's row_src).
   const int32_t* gather_rows;
+  // Fused un-rearrangement: when set (FWD2, routed groups, bf16), output row r of the
+  // permuted order is written at row scatter_rows[r] (its token-major slot t*k + j).
+  const int32_t* scatter_rows;
   // BWD1T: when w_rT is set, routed row q also gets dl_perm[q] * w_rT[e] (the router term
   // of the x-gradient, so that the un-rearrangement need not add it)
   const float* dl_perm;     // [Tk] score gradient of each permuted row

@@ -53,6 +53,7 @@ struct WsLayout {
   size_t dest_full;    // [T*k] int32   drop-and-pad: dropless position of every copy
   size_t row_src_full; // [T*k] int32   ... and token of every dropless position
   size_t offsets_full; // [E+1] int32   ... dropless expert offsets
+  size_t scatter_rows; // [T*k] int32   fused un-rearrangement: token-major slot of each row
   size_t total;
   int64_t n_chunks;
   int n_dgate_tiles;
@@ -85,6 +86,8 @@ cudaError_t launch_pad_rows(void* buf, int width, int dtype, const int32_t* offs
                             int C, int32_t* row_src, float* w_perm, cudaStream_t st);
 cudaError_t launch_permute_rows(const void* x, const int32_t* dest, const moe_dims& dm, void* x_perm,
                                 cudaStream_t st);
+// Fused un-rearrangement: scatter_rows[dest[c]] = c for the n = T*k dropless copies.
+cudaError_t launch_scatter_rows(const int32_t* dest, int64_t n, int32_t* scatter_rows, cudaStream_t st);
 cudaError_t launch_combine(const void* y_perm, const int32_t* dest, const float* topk_w,
                            const void* y_sh, const int32_t* idx, const float* dl_tok,
                            const float* w_rT, const moe_dims& dm, void* y, cudaStream_t st);

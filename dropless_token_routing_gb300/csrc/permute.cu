@@ -212,11 +212,23 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const T* __restrict__
   }
 }
 
+// ---------------------------------------------------------------- fused un-rearrangement
+// scatter_rows[dest[c]] = c: the token-major slot of every expert-order row (dropless).
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const int32_t* __restrict__ dest, int64_t n,
+                                                          int32_t* __restrict__ scatter_rows) {
+  for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < n; c += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t q = dest[c];
+    if (q >= 0) scatter_rows[q] = (int32_t)c;
+  }
+}
+
 // ---------------------------------------------------------------- a4: combine
 // y[t] = sum_j w_j y_perm[dest_j] (+ y_sh[t]) (+ sum_j dl_j W_r^T[e_j]) in fp32, in that
 // order, rounded once, 8 elements per lane per step. With k <= KMAX (no router term) the
 // k rows' vectors of a step (and the shared expert's) are all requested before the sums
 // start, so a warp keeps k + 1 loads in flight instead of one; the sums keep their order.
+// dest == nullptr: the rows are already in token-major order (copy j of token t at row
+// t*k + j, written there by the fused un-rearrangement), read as one contiguous block.
 template <typename T, bool ROUTER, int KMAX>
 __global__ void __launch_bounds__(256) combine_kernel(
     const T* __restrict__ y_perm, const int32_t* __restrict__ dest, const float* __restrict__ topk_w,
@@ -237,7 +249,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
       float wq = 0.f;
       if (lane < k) {
         const int64_t q = t * k + lane;
-        dq = dest[q];
+        dq = dest != nullptr ? dest[q] : (int)q;
         wq = topk_w != nullptr ? topk_w[q] : 1.f;
       }
       // every lane holds every copy's row and weight (uniform across the warp)
@@ -284,7 +296,7 @@ __global__ void __launch_bounds__(256) combine_kernel(
       float wq = 0.f, gq = 0.f;
       if (lane < k) {
         const int64_t q = t * k + lane;
-        dq = dest[q];
+        dq = dest != nullptr ? dest[q] : (int)q;
         wq = topk_w != nullptr ? topk_w[q] : 1.f;
         if (ROUTER) {
           eq = idx[q];
@@ -420,6 +432,14 @@ void combine_dispatch(const T* y_perm, const int32_t* dest, const float* topk_w,
                                                         dm.d, dm.k, y);
 }
 }  // namespace
+
+cudaError_t launch_scatter_rows(const int32_t* dest, int64_t n, int32_t* scatter_rows, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  TraceScope ts(TP_MISC, st);
+  scatter_rows_kernel<<<blocks, 256, 0, st>>>(dest, n, scatter_rows);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const void* y_perm, const int32_t* dest, const float* topk_w,
                            const void* y_sh, const int32_t* idx, const float* dl_tok,

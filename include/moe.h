@@ -86,16 +86,20 @@ typedef struct moe_dims {
    * zero padding. The permuted buffers (x_perm, row_src, w_perm, z, h, y_perm, dy_perm,
    * dz, dx_perm) then have R = E*C rows instead of R = T*k, and offsets[e] = e*C. */
   int32_t capacity;
-  /* enum moe_rearrange: how the bf16 dropless layer feeds the permuted token rows to the
-   * expert GEMMs. MOE_REARRANGE_COPY (0, default): rearranged copies in memory (x_perm,
-   * dy_perm). MOE_REARRANGE_GATHER (1): the copies are fused into the GEMMs' operand loads
-   * (TMA row gathers from x and dy by row_src). On GB300 the gathers make the GEMMs about
-   * 2.5x slower than the copies cost, so the copy is the default. fp32 layers and the
-   * drop-and-pad variant always use copies. */
+  /* enum moe_rearrange (flags): how the bf16 dropless layer moves token rows between token
+   * order and expert order around the expert GEMMs. MOE_REARRANGE_COPY (0, default):
+   * rearranged copies in memory (x_perm, dy_perm) and an un-rearranging combine that
+   * gathers each token's k expert rows from y_perm by dest. MOE_REARRANGE_GATHER (1): the
+   * rearrangement is fused into the GEMMs' operand loads (row gathers from x and dy by
+   * row_src). MOE_REARRANGE_SCATTER (2): moe_layer_fwd's second expert GEMM writes each
+   * output row at its token-major slot t*k + j instead of its expert-order row, so the
+   * combine reads every token's k rows as one contiguous block. Both together: 3. The
+   * results are identical in every form. fp32 layers and the drop-and-pad variant always use
+   * the copies. */
   int32_t rearrange;
 } moe_dims;
 
-enum moe_rearrange { MOE_REARRANGE_COPY = 0, MOE_REARRANGE_GATHER = 1 };
+enum moe_rearrange { MOE_REARRANGE_COPY = 0, MOE_REARRANGE_GATHER = 1, MOE_REARRANGE_SCATTER = 2 };
 
 /* Human-readable text of a status code (static string). */
 const char* moe_status_string(int status);

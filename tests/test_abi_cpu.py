@@ -58,6 +58,20 @@ def test_workspace_bytes_and_dims_validation():
     assert 4e9 < nb < 2e10
 
 
+def test_rearrange_flags_are_validated():
+    """moe_dims.rearrange takes the flags copy (0), gather (1), scatter (2) and both (3); the
+    scatter form reserves one int32 per token copy for the token-major slots."""
+    def with_rearrange(r, **kw):
+        d = dims(dtype=N.MOE_BF16, **kw)
+        d.rearrange = r
+        return d
+    sizes = {r: L.moe_workspace_bytes(ctypes.byref(with_rearrange(r))) for r in (0, 1, 2, 3)}
+    assert all(v > 256 for v in sizes.values())
+    assert sizes[2] >= sizes[0] + 4 * 256 * 2 and sizes[3] == sizes[2] and sizes[1] == sizes[0]
+    for bad in (-1, 4, 7):
+        assert L.moe_workspace_bytes(ctypes.byref(with_rearrange(bad))) == 0
+
+
 def _code(name):
     return N.STATUS_CODE[name]
 

@@ -313,7 +313,7 @@ def test_capacity_fullsize_permutation_and_sampled_tokens(run_capacity):
     assert _rel(_f64(g["dlogits"][toks]), dscores) <= TOL
 
 
-@pytest.mark.parametrize("rearrange,recompute", [(1, True), (0, True)])
+@pytest.mark.parametrize("rearrange,recompute", [(1, True), (0, True), (2, False), (3, True)])
 def test_fused_gather_at_full_size_matches_the_copies_bitwise(rearrange, recompute):
     """The Pangu-shaped layer at its full size with the rearrangement fused into the GEMMs'
     operand loads (row gathers from x and dY), or with selective recompute alone (x_perm and h

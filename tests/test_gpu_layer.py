@@ -147,23 +147,27 @@ def test_capacity_at_max_count_reproduces_dropless_rows():
 
 
 # ---------------------------------------------------------------- fused rearrangement
+@pytest.mark.parametrize("rearrange", [1, 2, 3])
 @pytest.mark.parametrize("case", ["pangu_small", "dsv3_small", "adversarial_small"])
-def test_fused_gather_layer_matches_oracle(case):
-    """MOE_REARRANGE_GATHER: the expert GEMMs gather their token rows from x / dy by row_src
-    (no rearranged copies of dY, x_perm kept only for the check) and still meet every bar."""
+def test_fused_rearrangement_layer_matches_oracle(case, rearrange):
+    """MOE_REARRANGE_GATHER (1): the expert GEMMs gather their token rows from x / dy by row_src
+    (no rearranged copies of dY, x_perm kept only for the check); MOE_REARRANGE_SCATTER (2):
+    the second expert GEMM writes its rows at their token-major slots and the combine reads
+    each token's k rows as one block; 3: both. Every form meets every bar."""
     from layer_check import check_layer
     name, over = CASES[case]
-    check_layer(make_workload(shrink(name, **over)), bwd=True, rearrange=1)
+    check_layer(make_workload(shrink(name, **over)), bwd=True, rearrange=rearrange)
 
 
-def test_fused_gather_matches_copies_bitwise():
-    """Gathered rows are the same bf16 values as the copied ones, fed in the same order: the
-    forward and dX results are bit-identical; the dW products agree to rounding (same
-    tiles, same order; checked bitwise too)."""
+@pytest.mark.parametrize("rearrange", [1, 2, 3])
+def test_fused_rearrangement_matches_copies_bitwise(rearrange):
+    """Gathered rows are the same bf16 values as the copied ones, fed in the same order, and the
+    token-major rows are the same values the combine gathered by dest, summed in the same
+    order: the forward, dX and dW results are bit-identical to the copy path."""
     from layer_check import run_gpu_layer
     w = make_workload(shrink("pangu_bf16", T=640, d=512, E=16, k=4, f=256, f_s=256))
     a, ga, e0 = run_gpu_layer(w)
-    b, gb, e1 = run_gpu_layer(w, rearrange=1)
+    b, gb, e1 = run_gpu_layer(w, rearrange=rearrange)
     assert e0 == 0 and e1 == 0
     assert torch.equal(a.y, b.y) and torch.equal(a.saved["z"], b.saved["z"])
     for n in ("dx", "dw13", "dw2", "dws13", "dws2", "dw_r"):
@@ -305,9 +309,9 @@ def _random_shapes(n, seed):
                    f_s=unit * rng.randint(1, 6) if S else 0)
         base = "pangu_bf16" if bf16 else "tiny_fp32"
         # the variants: dropless copies, drop-and-pad at a random capacity, fused row gathers
-        variant = rng.choice(["copy", "copy", "capacity", "gather"]) if bf16 else rng.choice(["copy", "capacity"])
+        variant = rng.choice(["copy", "copy", "capacity", "gather", "scatter"]) if bf16 else rng.choice(["copy", "capacity"])
         cap = max(1, int(cfg["T"] * k / E * rng.choice([0.5, 1.0, 1.5]))) if variant == "capacity" else 0
-        out.append((base, cfg, cap, 1 if variant == "gather" else 0))
+        out.append((base, cfg, cap, {"gather": 1, "scatter": 3}.get(variant, 0)))
     return out
 
 
@@ -315,7 +319,8 @@ def _random_shapes(n, seed):
 def test_layer_on_random_shapes(base, over, capacity, rearrange):
     """Seeded random shapes (ragged everything: T from 1 to 700, d and f at any multiple of the
     vector unit, E up to 257, k up to 9, 0-2 shared experts, both dtypes), in the dropless,
-    drop-and-pad and fused-gather forms, each against the oracle at the usual bars."""
+    drop-and-pad, fused-gather and fused gather + scatter forms, each against the oracle at
+    the usual bars."""
     from layer_check import check_layer
     cfg = shrink(base, **over)
     if cfg["S"] == 0:
