@@ -375,7 +375,8 @@ int moe_unpermute_combine(const void* y_perm, const int32_t* dest, const float* 
   MOE_TRY(check_dims(dims));
   const bool t0 = dims->T == 0;
   MOE_TRY(reqT(y_perm, t0));
-  MOE_TRY(reqT(dest, t0));
+  MOE_TRY(opt(dest));    // NULL: y_perm rows in token-major order
+  if (dest == nullptr && dims->capacity > 0) return MOE_ERR_NULL_POINTER;
   MOE_TRY(opt(topk_w));
   MOE_TRY(opt(y_sh));
   MOE_TRY(reqT(y, t0));

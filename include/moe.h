@@ -186,7 +186,9 @@ int moe_grouped_swiglu_fwd(const void* x_perm, const void* x, const void* w13, c
  * (Huawei MoE training-operator article, Fig. 3; Pangu Ultra MoE article, weighted sum):
  *   y_t = sum_{j=0..k-1} topk_w[t,j] * y_perm[dest[t*k+j]] + y_sh[t]
  * summed in fp32 in that order and rounded once. topk_w NULL = weight 1; y_sh may be NULL.
- * y_perm [T*k, d], dest [T*k] -> y [T, d]. */
+ * y_perm [T*k, d], dest [T*k] -> y [T, d]. dest NULL: y_perm is already in token-major
+ * order (row t*k + j holds copy j of token t, as moe_layer_fwd's second expert GEMM writes
+ * it under MOE_REARRANGE_SCATTER); a dropped copy (drop-and-pad) needs dest. */
 int moe_unpermute_combine(const void* y_perm, const int32_t* dest, const float* topk_w,
                           const void* y_sh, const moe_dims* dims, void* y, moe_stream_t stream);
 

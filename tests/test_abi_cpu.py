@@ -103,6 +103,10 @@ def test_host_argument_errors():
     assert L.moe_grouped_swiglu_fwd(GOOD, None, GOOD, GOOD, GOOD, GOOD, GOOD, ctypes.byref(ds), GOOD,
                                     GOOD, GOOD, GOOD, GOOD, GOOD, GOOD, ws_s, None) == _code("MOE_ERR_NULL_POINTER")
     assert L.moe_unpermute_combine(GOOD, GOOD, BAD, None, ctypes.byref(d), GOOD, None) == _code("MOE_ERR_MISALIGNED")
+    # dest NULL (token-major rows) is refused for drop-and-pad, where copies can be dropped
+    dc = dims()
+    dc.capacity = 4
+    assert L.moe_unpermute_combine(GOOD, None, None, None, ctypes.byref(dc), GOOD, None) == _code("MOE_ERR_NULL_POINTER")
     assert L.moe_route_topk_bwd(GOOD, GOOD, GOOD, 4, 8, 9, GOOD, None) == _code("MOE_ERR_BAD_TOPK")
     # layer calls: router weights or logits must be given; grads need dlogits without W_r
     p = N.LayerParams(None, None, GOOD, GOOD, None, None)

@@ -100,6 +100,11 @@ def test_permute_matches_stable_counting_sort(T, E, k, skew):
     A.unpermute_combine(x_perm, dest, torch.as_tensor(gate).cuda(), x.cuda(), dims, y)
     ref = O.as_f64(x) * (gate.double().sum(1, keepdim=True).numpy() + 1.0)
     assert np.linalg.norm(O.as_f64(y) - ref) / np.linalg.norm(ref) <= 5e-3
+    # the same rows in token-major order (dest NULL) give the same y bit for bit
+    tok_major = x_perm[dest.long()]
+    y2 = torch.empty_like(y)
+    A.unpermute_combine(tok_major, None, torch.as_tensor(gate).cuda(), x.cuda(), dims, y2)
+    assert torch.equal(y, y2)
 
 
 @pytest.mark.parametrize("T,E,k,C", [(1000, 24, 3, 100), (3000, 256, 8, 90), (4097, 64, 6, 1),
