@@ -348,6 +348,54 @@ def fused_rearrange(params, cfg, w, args, stream):
     return dict(out["gather"], variants=out)
 
 
+def balance_statistics(cfg, w, logits, ws, stream, peaks, reps=50):
+    """Routing with the micro-batch balance statistics: the top-k call and the statistics call
+    one after the other, against the single call that takes both from one read of the scores.
+    Each variant's `reps` calls are captured in a CUDA graph and replayed, so that the device
+    time is measured rather than the host's call rate; the scores stay in L2 between
+    repetitions, as in the step, where the router writes them just before."""
+    import torch
+    from dropless_token_routing_gb300 import api as A
+    T, E, k = cfg["T"], cfg["E"], cfg["k"]
+    dev = logits.device
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    gw = torch.empty(T, k, device=dev)
+    cnt = torch.empty(E, dtype=torch.int32, device=dev)
+    P = torch.empty(E, device=dev)
+    aux = torch.empty(1, device=dev)
+    alpha = 1e-2
+    runs = {
+        "topk_only": lambda: A.route_topk(logits, w.bias, k, idx, gw, cnt, ws),
+        "topk_then_balance": lambda: (A.route_topk(logits, w.bias, k, idx, gw, cnt, ws),
+                                      A.route_balance(logits, w.bias, cnt, k, alpha, P, aux, ws)),
+        "fused": lambda: A.route_topk_balance(logits, w.bias, k, alpha, idx, gw, cnt, P, aux, ws),
+    }
+    out = {}
+    for name, fn in runs.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        out[name] = {"us": round(a.elapsed_time(b) / reps * 1e3, 2)}
+        del g
+    # bytes of the fused call: the scores once, gates and indices out, the partial rows
+    nbytes = T * E * 4 + T * k * 8 + min(512, (T + 7) // 8) * E * 4 * 2
+    us = out["fused"]["us"]
+    out["fused"].update({"bytes": nbytes, "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                         "frac_hbm": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 3)})
+    return out
+
+
 # --------------------------------------------------------------------------- summaries
 def summarize(cfg, trace, steps, counts, peaks):
     """Per-kernel table, grouped-GEMM totals and routing statistics of a traced run of
@@ -747,6 +795,8 @@ def main():
         line["drop_and_pad"] = drop_and_pad(factors, params, cfg, w, cnt, args, stream)
     if args.fused_rearrange and cfg["dtype"] == "bf16":
         line["fused_rearrange"] = fused_rearrange(params, cfg, w, args, stream)
+    line["balance_statistics"] = balance_statistics(
+        cfg, w, (li if li is not None else layer.saved["logits"]), layer.ws, stream, peaks)
     others = [n for n in args.other_workloads.split(",") if n.strip() and n.strip() != args.config]
     if others and not args.shrink:
         del layer, params, w, x, dy, li, d_in, h_x, h_dy, h_li, h_y, h_dx

@@ -85,6 +85,8 @@ _SIGS = {
                                    P, c_size_t, P]),
     "moe_route_topk_bwd": (c_int, [P, P, P, c_int64, c_int32, c_int32, P, P]),
     "moe_route_balance": (c_int, [P, P, P, c_int64, c_int32, c_int32, ctypes.c_float, P, P, P, c_size_t, P]),
+    "moe_route_topk_balance": (c_int, [P, P, c_int64, c_int32, c_int32, ctypes.c_float, P, P, P, P, P, P,
+                                       c_size_t, P]),
     "moe_route_balance_bwd": (c_int, [P, P, P, c_int64, c_int32, c_int32, ctypes.c_float, ctypes.c_float, P, P]),
     "moe_route_balance_seq": (c_int, [P, P, P, c_int64, c_int32, c_int32, c_int64, ctypes.c_float, P, P, P, P,
                                       c_size_t, P]),

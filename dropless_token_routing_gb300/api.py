@@ -136,6 +136,14 @@ def route_balance(logits, bias, counts, k, alpha, prob_mean, aux_loss, ws: Works
             "moe_route_balance")
 
 
+def route_topk_balance(logits, bias, k, alpha, topk_idx, topk_w, counts, prob_mean, aux_loss, ws: Workspace,
+                       stream=None):
+    T, E = logits.shape
+    N.check(N.lib().moe_route_topk_balance(_p(logits), _p(bias), T, E, k, float(alpha), _p(topk_idx),
+                                           _p(topk_w), _p(counts), _p(prob_mean), _p(aux_loss), ws.ptr,
+                                           ws.nbytes, _s(stream)), "moe_route_topk_balance")
+
+
 def route_balance_bwd(logits, bias, counts, k, alpha, grad, dlogits, stream=None):
     T, E = logits.shape
     N.check(N.lib().moe_route_balance_bwd(_p(logits), _p(bias), _p(counts), T, E, k, float(alpha),

@@ -476,7 +476,8 @@ int moe_route_balance(const float* logits, const float* bias, const int32_t* cou
   if (k < 1 || k > E || k > kMaxK) return MOE_ERR_BAD_TOPK;
   if (ws == nullptr) return MOE_ERR_NULL_POINTER;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_MISALIGNED;
-  if (ws_bytes < 256 + sizeof(float) * (size_t)balance_blocks(T) * E) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < 256 + sizeof(float) * ((size_t)balance_blocks(T) * E + balance_term_parts(E)))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
   MOE_TRY(req(logits));
   MOE_TRY(opt(bias));
   MOE_TRY(req(counts));
@@ -485,6 +486,30 @@ int moe_route_balance(const float* logits, const float* bias, const int32_t* cou
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
   MOE_LAUNCH(launch_balance(logits, bias, counts, T, E, k, alpha, part, prob_mean, aux_loss,
                             (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+int moe_route_topk_balance(const float* logits, const float* bias, int64_t T, int32_t E, int32_t k,
+                           float alpha, int32_t* topk_idx, float* topk_w, int32_t* counts, float* prob_mean,
+                           float* aux_loss, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (E < 1 || E > kMaxE || T < 1 || T > (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
+  if (k < 1 || k > E || k > kMaxK) return MOE_ERR_BAD_TOPK;
+  if (ws == nullptr) return MOE_ERR_NULL_POINTER;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_MISALIGNED;
+  if (ws_bytes < 256 + sizeof(float) * ((size_t)balance_blocks(T) * E + balance_term_parts(E)))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  MOE_TRY(req(logits));
+  MOE_TRY(opt(bias));
+  MOE_TRY(req(topk_idx));
+  MOE_TRY(req(topk_w));
+  MOE_TRY(req(counts));
+  MOE_TRY(opt(prob_mean));
+  MOE_TRY(req(aux_loss));
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st) != cudaSuccess) return MOE_ERR_CUDA;
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
+  MOE_LAUNCH(launch_route_topk_balance(logits, bias, T, E, k, alpha, topk_idx, topk_w, counts, part, prob_mean,
+                                       aux_loss, st));
   return MOE_OK;
 }
 

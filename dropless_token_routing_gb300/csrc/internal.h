@@ -95,9 +95,15 @@ cudaError_t launch_router_split(const float* w_r, int d, int E, void* w_split, c
 cudaError_t launch_router_reduce(const float* part, int64_t T, int E, int nsplit, float* logits,
                                  cudaStream_t st);
 int balance_blocks(int64_t T);
+int balance_term_parts(int E);   // the loss shares after the partial rows (one per 32 experts)
 cudaError_t launch_balance(const float* logits, const float* bias, const int32_t* counts, int64_t T,
                            int E, int k, float alpha, float* part, float* prob_mean, float* aux_loss,
                            cudaStream_t st);
+// launch_route_topk with the balance statistics of launch_balance fused in (same results,
+// bit for bit); part: [balance_blocks(T)][E] fp32, then balance_term_parts(E) fp32.
+cudaError_t launch_route_topk_balance(const float* logits, const float* bias, int64_t T, int E, int k,
+                                      float alpha, int32_t* idx, float* w, int32_t* counts, float* part,
+                                      float* prob_mean, float* aux_loss, cudaStream_t st);
 cudaError_t launch_balance_bwd(const float* logits, const float* bias, const int32_t* counts,
                                int64_t T, int E, int64_t group_len, float scale, float* dlogits,
                                cudaStream_t st);

@@ -69,27 +69,56 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const TX* __restrict
   }
 }
 
+// Order-preserving map of a float (not NaN) to uint32: a > b as floats iff key(a) > key(b);
+// +0 and -0 get different keys, so callers pass x + 0.f (which is +0 for both zeros).
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 // ---------------------------------------------------------------- a1: fused route
 // One warp per token. Lane l holds the scores of experts l, l+32, ... (V per lane).
 // k rounds of a warp arg-max under the order (score descending, index ascending).
-template <int V>
+// BAL: the balance statistics' softmax sums are taken from the same registers (the scores are
+// read once): each lane keeps fp32 sums of the full softmax for its experts over the warp's
+// tokens, and the block writes one partial row part[blockIdx.x][E], its warps summed in order.
+// With the grid of balance_partial_kernel the partial rows are the same bits as that kernel's.
+template <int V, bool BAL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits,
                                                          const float* __restrict__ bias, int64_t T,
                                                          int E, int k, int32_t* __restrict__ idx,
                                                          float* __restrict__ w,
-                                                         int32_t* __restrict__ counts) {
-  extern __shared__ int hist[];
+                                                         int32_t* __restrict__ counts,
+                                                         float* __restrict__ part) {
+  extern __shared__ int hist[];   // [E] counts, then (BAL) [8][E] fp32 warp sums
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < T; t += (int64_t)gridDim.x * nw) {
+  float acc[BAL ? V : 1];
+#pragma unroll
+  for (int i = 0; i < (BAL ? V : 1); ++i) acc[i] = 0.f;
+  // the next token's scores are loaded while this token's are ranked
+  const int64_t stride = (int64_t)gridDim.x * nw;
+  float nxt[V];
+  auto load_row = [&](int64_t t) {
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = lane + 32 * i;
+      nxt[i] = (t < T && e < E) ? __ldg(logits + t * E + e) : 0.f;
+    }
+  };
+  load_row((int64_t)blockIdx.x * nw + warp);
+  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < T; t += stride) {
     float v[V];
     uint32_t taken = 0;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int e = lane + 32 * i;
       if (e < E) {
-        float s = __ldg(logits + t * E + e);
+        float s = nxt[i];
         if (bias != nullptr) s = s + __ldg(bias + e);   // one fp32 rounding
         v[i] = s;
       } else {
@@ -97,37 +126,60 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
         taken |= 1u << i;
       }
     }
-    float my_v = 0.f;
-    int my_i = 0;
-    for (int j = 0; j < k; ++j) {
-      float bv = -FLT_MAX;
-      int bi = 0x7fffffff;
-      bool have = false;
+    load_row(t + stride);
+    if constexpr (BAL) {
+      // full softmax of the row, in the same operations as balance_partial_kernel
+      float mx = -FLT_MAX;
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+        if (lane + 32 * i < E) mx = fmaxf(mx, v[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float p[V];
+      float z = 0.f;
 #pragma unroll
       for (int i = 0; i < V; ++i) {
-        if (!((taken >> i) & 1u) && (!have || v[i] > bv)) {  // ascending index: ties keep lower
-          bv = v[i];
-          bi = lane + 32 * i;
-          have = true;
-        }
+        p[i] = (lane + 32 * i < E) ? expf(v[i] - mx) : 0.f;
+        z += p[i];
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        const int oh = __shfl_xor_sync(0xffffffffu, (int)have, o);
-        if (oh && (!have || ov > bv || (ov == bv && oi < bi))) {
-          bv = ov;
-          bi = oi;
-          have = true;
+      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      const float inv = 1.f / z;
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = fmaf(p[i], inv, acc[i]);
+    }
+    // selection on order-preserving integer keys of the scores (-0 taken as +0, so that the two
+    // zeros tie as they do in a float comparison); a chosen or absent expert has key 0, below
+    // every finite score. Round j: each lane's best key (its lowest expert on a tie), the
+    // warp's maximum key, then the lowest expert index holding it: two warp reductions.
+    uint32_t key[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) key[i] = ((taken >> i) & 1u) ? 0u : order_key(v[i] + 0.f);
+    uint32_t my_key = 0;
+    int my_i = 0;
+    for (int j = 0; j < k; ++j) {
+      uint32_t kb = 0;
+      int ib = 0;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        if (key[i] > kb) {
+          kb = key[i];
+          ib = i;
         }
       }
-      if (lane == (bi & 31)) taken |= 1u << (bi >> 5);
+      const uint32_t wmax = __reduce_max_sync(0xffffffffu, kb);
+      const uint32_t wi = __reduce_min_sync(0xffffffffu, kb == wmax ? (uint32_t)(lane + 32 * ib) : 0xffffffffu);
+      if (lane == (int)(wi & 31u)) {
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+          if (i == (int)(wi >> 5)) key[i] = 0u;
+      }
       if (lane == j) {
-        my_v = bv;
-        my_i = bi;
+        my_key = wmax;
+        my_i = (int)wi;
       }
     }
+    const float my_v = key_value(my_key);
     const float m = __shfl_sync(0xffffffffu, my_v, 0);   // top-1 = row maximum
     const float ex = lane < k ? expf(my_v - m) : 0.f;
     float sum = ex;
@@ -139,9 +191,23 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
       atomicAdd(&hist[my_i], 1);
     }
   }
+  if constexpr (BAL) {
+    float* wsum = reinterpret_cast<float*>(hist + E);
+#pragma unroll
+    for (int i = 0; i < V; ++i)
+      if (lane + 32 * i < E) wsum[warp * E + lane + 32 * i] = acc[i];
+  }
   __syncthreads();
   for (int i = threadIdx.x; i < E; i += blockDim.x)
     if (hist[i] != 0) atomicAdd(counts + i, hist[i]);
+  if constexpr (BAL) {
+    const float* wsum = reinterpret_cast<const float*>(hist + E);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      float s = 0.f;
+      for (int w8 = 0; w8 < nw; ++w8) s += wsum[w8 * E + e];
+      part[(int64_t)blockIdx.x * E + e] = s;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- router backward
@@ -245,7 +311,18 @@ __global__ void __launch_bounds__(256) balance_partial_kernel(const float* __res
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
-  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < T; t += (int64_t)gridDim.x * nw) {
+  // the next token's scores are loaded while this token's are summed
+  const int64_t stride = (int64_t)gridDim.x * nw;
+  float nxt[V];
+  auto load_row = [&](int64_t t) {
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = lane + 32 * i;
+      nxt[i] = (t < T && e < E) ? __ldg(logits + t * E + e) : 0.f;
+    }
+  };
+  load_row((int64_t)blockIdx.x * nw + warp);
+  for (int64_t t = (int64_t)blockIdx.x * nw + warp; t < T; t += stride) {
     float v[V];
     float m = -FLT_MAX;
 #pragma unroll
@@ -253,12 +330,13 @@ __global__ void __launch_bounds__(256) balance_partial_kernel(const float* __res
       const int e = lane + 32 * i;
       v[i] = -FLT_MAX;
       if (e < E) {
-        float s = __ldg(logits + t * E + e);
+        float s = nxt[i];
         if (bias != nullptr) s = s + __ldg(bias + e);
         v[i] = s;
         m = fmaxf(m, s);
       }
     }
+    load_row(t + stride);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float z = 0.f;
@@ -285,31 +363,44 @@ __global__ void __launch_bounds__(256) balance_partial_kernel(const float* __res
 }
 
 // P_e = (sum over block rows) / T;  L_aux = alpha * E / (T * k) * sum_e counts_e * P_e.
+// Block b takes experts 32b .. 32b+31: thread (j, el) sums slice j of expert 32b + el (block
+// rows j, j + 32, ..., ascending; a warp reads 32 consecutive experts of a row), warp 0 sums
+// the 32 slices in order, writes P and the block's share of the loss sum (its experts in a
+// fixed butterfly order). balance_loss_kernel adds the shares in block order.
 __global__ void __launch_bounds__(1024) balance_final_kernel(const float* __restrict__ part,
                                                              int nblocks, const int32_t* __restrict__ counts,
-                                                             int64_t T, int E, int k, float alpha,
+                                                             int64_t T, int E,
                                                              float* __restrict__ prob_mean,
-                                                             float* __restrict__ aux_loss) {
-  __shared__ float red[32];
-  const int e = threadIdx.x;
-  float term = 0.f;
-  if (e < E) {
-    float s = 0.f;
-    for (int b = 0; b < nblocks; ++b) s += part[(int64_t)b * E + e];
-    const float P = s / (float)T;
-    if (prob_mean != nullptr) prob_mean[e] = P;
-    term = (float)counts[e] * P;
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
-  if (lane == 0) red[warp] = term;
+                                                             float* __restrict__ term_part) {
+  __shared__ float slice[32][33];
+  const int el = threadIdx.x & 31, j = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + el;
+  float s = 0.f;
+  if (e < E)
+    for (int b = j; b < nblocks; b += 32) s += part[(int64_t)b * E + e];
+  slice[j][el] = s;
   __syncthreads();
-  if (threadIdx.x == 0 && aux_loss != nullptr) {
-    float s = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
-    aux_loss[0] = alpha * (float)E / ((float)T * (float)k) * s;
+  if (j == 0) {
+    float term = 0.f;
+    if (e < E) {
+      float tot = 0.f;
+      for (int q = 0; q < 32; ++q) tot += slice[q][el];
+      const float P = tot / (float)T;
+      if (prob_mean != nullptr) prob_mean[e] = P;
+      term = (float)counts[e] * P;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+    if (el == 0) term_part[blockIdx.x] = term;
   }
+}
+
+__global__ void balance_loss_kernel(const float* __restrict__ term_part, int nparts, int64_t T, int E, int k,
+                                    float alpha, float* __restrict__ aux_loss) {
+  if (threadIdx.x != 0 || aux_loss == nullptr) return;
+  float s = 0.f;
+  for (int i = 0; i < nparts; ++i) s += term_part[i];
+  aux_loss[0] = alpha * (float)E / ((float)T * (float)k) * s;
 }
 
 // Sequence-level statistics: groups of group_len consecutive tokens. Block (c, g) sums the
@@ -614,9 +705,9 @@ cudaError_t launch_route_topk(const float* logits, const float* bias, int64_t T,
   const size_t sm = sizeof(int) * E;
   const int V = (E + 31) / 32;
   TraceScope ts(TP_ROUTE_TOPK, st);
-#define MOE_ROUTE_CASE(VV)                                                                   \
-  route_topk_kernel<VV><<<(unsigned)blocks, threads, sm, st>>>(logits, bias, T, E, k, idx, w, \
-                                                               counts);
+#define MOE_ROUTE_CASE(VV)                                                                          \
+  route_topk_kernel<VV, false><<<(unsigned)blocks, threads, sm, st>>>(logits, bias, T, E, k, idx, w, \
+                                                                      counts, nullptr);
   if (V <= 1) { MOE_ROUTE_CASE(1) }
   else if (V <= 2) { MOE_ROUTE_CASE(2) }
   else if (V <= 4) { MOE_ROUTE_CASE(4) }
@@ -658,9 +749,12 @@ cudaError_t launch_router_reduce(const float* part, int64_t T, int E, int nsplit
   return cudaGetLastError();
 }
 
+int balance_term_parts(int E) { return (E + 31) / 32; }
+
 int balance_blocks(int64_t T) {
+  constexpr int64_t kMaxBlocks = 512;
   int64_t b = (T + 7) / 8;
-  return (int)(b < 256 ? (b < 1 ? 1 : b) : 256);
+  return (int)(b < kMaxBlocks ? (b < 1 ? 1 : b) : kMaxBlocks);
 }
 
 #define MOE_V_DISPATCH(E, CALL)            \
@@ -674,6 +768,19 @@ int balance_blocks(int64_t T) {
     else { constexpr int VV = 32; CALL; } \
   } while (0)
 
+// part: nb rows of E partial sums, followed by room for balance_term_parts(E) floats.
+static cudaError_t launch_balance_final(float* part, int nb, const int32_t* counts, int64_t T, int E, int k,
+                                        float alpha, float* prob_mean, float* aux_loss, cudaStream_t st) {
+  const int nt = balance_term_parts(E);
+  float* term_part = part + (size_t)nb * E;
+  TraceScope ts(TP_MISC, st);
+  balance_final_kernel<<<nt, 1024, 0, st>>>(part, nb, counts, T, E, prob_mean, term_part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  balance_loss_kernel<<<1, 32, 0, st>>>(term_part, nt, T, E, k, alpha, aux_loss);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_balance(const float* logits, const float* bias, const int32_t* counts, int64_t T,
                            int E, int k, float alpha, float* part, float* prob_mean, float* aux_loss,
                            cudaStream_t st) {
@@ -684,9 +791,24 @@ cudaError_t launch_balance(const float* logits, const float* bias, const int32_t
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  TraceScope ts(TP_MISC, st);
-  balance_final_kernel<<<1, 1024, 0, st>>>(part, nb, counts, T, E, k, alpha, prob_mean, aux_loss);
-  return cudaGetLastError();
+  return launch_balance_final(part, nb, counts, T, E, k, alpha, prob_mean, aux_loss, st);
+}
+
+cudaError_t launch_route_topk_balance(const float* logits, const float* bias, int64_t T, int E, int k,
+                                      float alpha, int32_t* idx, float* w, int32_t* counts, float* part,
+                                      float* prob_mean, float* aux_loss, cudaStream_t st) {
+  // the grid of balance_partial_kernel, so that the partial rows (and everything after them)
+  // are the same bits as the separate statistics call
+  const int nb = balance_blocks(T);
+  const size_t sm = sizeof(int) * E + sizeof(float) * 8 * E;
+  {
+    TraceScope ts(TP_ROUTE_TOPK, st);
+    MOE_V_DISPATCH(E, (route_topk_kernel<VV, true><<<nb, 256, sm, st>>>(logits, bias, T, E, k, idx, w, counts,
+                                                                         part)));
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_balance_final(part, nb, counts, T, E, k, alpha, prob_mean, aux_loss, st);
 }
 
 cudaError_t launch_balance_bwd(const float* logits, const float* bias, const int32_t* counts,

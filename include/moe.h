@@ -232,10 +232,22 @@ int moe_route_topk_bwd(const int32_t* topk_idx, const float* topk_w, const float
  *   L_aux = alpha * E * sum_e f_e P_e
  * logits [T][E] fp32, bias [E] or NULL, counts [E] int32 (from moe_route_topk) ->
  * prob_mean [E] fp32 (or NULL), aux_loss [1] fp32 (device). Fixed-order reductions
- * (deterministic). ws: >= 256 + 4*E*min(256, ceil(T/8)) bytes, 256-byte aligned. T >= 1. */
+ * (deterministic). ws: >= 256 + 4*(E*min(512, ceil(T/8)) + ceil(E/32)) bytes, 256-byte aligned. T >= 1. */
 int moe_route_balance(const float* logits, const float* bias, const int32_t* counts, int64_t T,
                       int32_t E, int32_t k, float alpha, float* prob_mean, float* aux_loss, void* ws,
                       size_t ws_bytes, moe_stream_t stream);
+
+/* moe_route_topk and moe_route_balance in one pass over the scores (the balance statistics
+ * fused into the routing kernel: the Pangu Ultra MoE tech-report article's load-balancing
+ * section computes them from the same router scores). Each warp takes the full softmax of its
+ * token's scores from the registers the top-k reads, so the scores are read once.
+ * logits [T][E] fp32, bias [E] fp32 or NULL -> topk_idx [T][k], topk_w [T][k], counts [E]
+ * (zeroed and filled), prob_mean [E] (or NULL), aux_loss [1]: the same bits as moe_route_topk
+ * followed by moe_route_balance with the same alpha. T >= 1; ws as for moe_route_balance
+ * (>= 256 + 4*(E*min(512, ceil(T/8)) + ceil(E/32)) bytes, 256-byte aligned). */
+int moe_route_topk_balance(const float* logits, const float* bias, int64_t T, int32_t E, int32_t k,
+                           float alpha, int32_t* topk_idx, float* topk_w, int32_t* counts, float* prob_mean,
+                           float* aux_loss, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Gradient of grad * L_aux w.r.t. the scores, ADDED into dlogits [T][E] (counts constant):
  *   dlogits[t,e] += grad * alpha * E / (T*T*k) * p_te * (counts_e - sum_e' counts_e' p_te'). */

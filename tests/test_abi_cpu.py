@@ -108,6 +108,17 @@ def test_host_argument_errors():
     dc.capacity = 4
     assert L.moe_unpermute_combine(GOOD, None, None, None, ctypes.byref(dc), GOOD, None) == _code("MOE_ERR_NULL_POINTER")
     assert L.moe_route_topk_bwd(GOOD, GOOD, GOOD, 4, 8, 9, GOOD, None) == _code("MOE_ERR_BAD_TOPK")
+    # routing with the balance statistics: T >= 1, the statistics' workspace, a loss output
+    rb = L.moe_route_topk_balance
+    a = 0.01
+    assert rb(GOOD, None, 0, 8, 2, a, GOOD, GOOD, GOOD, None, GOOD, GOOD, 4096, None) == _code("MOE_ERR_BAD_DIMS")
+    assert rb(GOOD, None, 16, 8, 9, a, GOOD, GOOD, GOOD, None, GOOD, GOOD, 4096, None) == _code("MOE_ERR_BAD_TOPK")
+    assert rb(GOOD, None, 16, 8, 2, a, GOOD, GOOD, GOOD, None, None, GOOD, 4096, None) == _code("MOE_ERR_NULL_POINTER")
+    assert rb(GOOD, None, 16, 8, 2, a, GOOD, GOOD, GOOD, BAD, GOOD, GOOD, 4096, None) == _code("MOE_ERR_MISALIGNED")
+    # 16 tokens -> 2 partial rows of 8 experts and one loss share: 256 + 68 bytes
+    assert rb(GOOD, None, 16, 8, 2, a, GOOD, GOOD, GOOD, None, GOOD, GOOD, 256 + 67, None) == \
+        _code("MOE_ERR_WORKSPACE_TOO_SMALL")
+    assert rb(GOOD, None, 16, 8, 2, a, GOOD, GOOD, GOOD, None, GOOD, GOOD + 16, 4096, None) == _code("MOE_ERR_MISALIGNED")
     # layer calls: router weights or logits must be given; grads need dlogits without W_r
     p = N.LayerParams(None, None, GOOD, GOOD, None, None)
     s = N.LayerSaved(*([GOOD] * 13))

@@ -270,6 +270,41 @@ def test_balance_statistics_and_gradient_match_oracle():
     assert torch.all((d.cpu() - expect).abs() <= tol)
 
 
+@pytest.mark.parametrize("T,E,k,bias", [(1, 8, 2, False), (1000, 24, 3, True), (2053, 64, 6, True),
+                                         (8192, 256, 8, True), (3000, 1000, 32, False)])
+def test_route_with_fused_balance_is_bitwise_the_two_calls(T, E, k, bias):
+    """moe_route_topk_balance gives the bits of moe_route_topk followed by moe_route_balance
+    (indices, gates, counts, mean probabilities, loss), and the statistics match the oracle."""
+    A = _api()
+    alpha = 0.01
+    g = torch.Generator().manual_seed(T + E)
+    L = torch.randn(T, E, generator=g) * 2
+    b = torch.randn(E, generator=g) * 0.5 if bias else None
+    dims = A.make_dims(T, 64, E, k, 64, dtype=torch.float32)
+    ws = A.Workspace(dims)
+    Lg, bg = L.cuda(), (b.cuda() if bias else None)
+
+    def outs():
+        return (torch.empty(T, k, dtype=torch.int32, device="cuda"), torch.empty(T, k, device="cuda"),
+                torch.empty(E, dtype=torch.int32, device="cuda"), torch.empty(E, device="cuda"),
+                torch.empty(1, device="cuda"))
+    i1, w1, c1, P1, a1 = outs()
+    A.route_topk(Lg, bg, k, i1, w1, c1, ws)
+    A.route_balance(Lg, bg, c1, k, alpha, P1, a1, ws)
+    i2, w2, c2, P2, a2 = outs()
+    A.route_topk_balance(Lg, bg, k, alpha, i2, w2, c2, P2, a2, ws)
+    torch.cuda.synchronize()
+    for u, v in ((i1, i2), (w1, w2), (c1, c2), (P1, P2), (a1, a2)):
+        assert torch.equal(u, v)
+    s32 = O.selection_scores(L.numpy(), b.numpy() if bias else None)
+    idx, _ = O.route_topk(s32, k)
+    assert np.array_equal(i2.cpu().numpy(), idx)
+    counts = O.expert_counts(idx, E)
+    P_ref, L_ref = O.balance_loss(s32, counts, k, alpha)
+    assert np.linalg.norm(P2.cpu().double().numpy() - P_ref) / np.linalg.norm(P_ref) <= 1e-5
+    assert abs(a2.item() - L_ref) / abs(L_ref) <= 1e-5
+
+
 @pytest.mark.parametrize("T,E,k,L", [(1024, 64, 6, 256), (1000, 24, 3, 1000), (4096, 256, 8, 512)])
 def test_balance_sequence_level_matches_oracle(T, E, k, L):
     """moe_route_balance_seq / _bwd (groups of L consecutive tokens) against the oracle."""
