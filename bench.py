@@ -535,6 +535,8 @@ def main():
                     help="the timed step's rearrangement: rearranged copies (default), row gathers "
                          "fused into the expert GEMMs (with selective recompute), the second GEMM "
                          "writing token-major rows for the combine, or both")
+    ap.add_argument("--no-balance-statistics", dest="balance_statistics", action="store_false",
+                    help="skip the timing of the routing forms with balance statistics")
     ap.add_argument("--no-fused-rearrange", dest="fused_rearrange", action="store_false",
                     help="skip the timing of the fused-rearrangement variant (rank 0, after the "
                          "main measurement)")
@@ -795,8 +797,9 @@ def main():
         line["drop_and_pad"] = drop_and_pad(factors, params, cfg, w, cnt, args, stream)
     if args.fused_rearrange and cfg["dtype"] == "bf16":
         line["fused_rearrange"] = fused_rearrange(params, cfg, w, args, stream)
-    line["balance_statistics"] = balance_statistics(
-        cfg, w, (li if li is not None else layer.saved["logits"]), layer.ws, stream, peaks)
+    if args.balance_statistics:
+        line["balance_statistics"] = balance_statistics(
+            cfg, w, (li if li is not None else layer.saved["logits"]), layer.ws, stream, peaks)
     others = [n for n in args.other_workloads.split(",") if n.strip() and n.strip() != args.config]
     if others and not args.shrink:
         del layer, params, w, x, dy, li, d_in, h_x, h_dy, h_li, h_y, h_dx
