@@ -111,16 +111,17 @@ int check_dims(const moe_dims* d) {
   if (d == nullptr) return MOE_ERR_NULL_POINTER;
   if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED_DTYPE;
   if (d->k < 1 || d->k > kMaxK || (d->E >= 1 && d->k > d->E)) return MOE_ERR_BAD_TOPK;
-  if (d->T < 0 || d->E < 1 || d->E > kMaxE || d->d < 1 || d->f < 1 || d->S < 0 ||
-      d->S > kMaxShared)
+  if (d->T < 0 || d->T > (int64_t)0x7fffffff || d->E < 1 || d->E > kMaxE || d->d < 1 || d->f < 1 ||
+      d->S < 0 || d->S > kMaxShared)
     return MOE_ERR_BAD_DIMS;
   if (d->S > 0 && d->f_s < 1) return MOE_ERR_BAD_DIMS;
   const int unit = d->dtype == MOE_BF16 ? 64 : 8;
   if (d->d % unit != 0 || d->f % unit != 0 || (d->S > 0 && d->f_s % unit != 0)) return MOE_ERR_BAD_DIMS;
   if (d->capacity < 0 || (int64_t)d->capacity * d->E >= (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
   if (d->rearrange < 0 || d->rearrange > (MOE_REARRANGE_GATHER | MOE_REARRANGE_SCATTER)) return MOE_ERR_BAD_DIMS;
+  // T is below 2^31 here, so these products fit in 64 bits
   const int64_t rows = d->T * (int64_t)d->k + perm_rows(*d) + (int64_t)d->S * d->T;
-  if (d->T > (int64_t)0x7fffffff || rows >= (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
+  if (rows >= (int64_t)0x7fffffff) return MOE_ERR_BAD_DIMS;
   return MOE_OK;
 }
 

@@ -52,6 +52,8 @@ def test_workspace_bytes_and_dims_validation():
     assert L.moe_workspace_bytes(ctypes.byref(dims(d=100))) == 0          # fp32 needs d % 8
     assert L.moe_workspace_bytes(ctypes.byref(dims(dtype=N.MOE_BF16, d=96))) == 0  # bf16 d % 64
     assert L.moe_workspace_bytes(ctypes.byref(dims(T=-1))) == 0
+    assert L.moe_workspace_bytes(ctypes.byref(dims(T=2**31))) == 0        # T must fit in int32
+    assert L.moe_workspace_bytes(ctypes.byref(dims(T=2**62, k=8))) == 0   # rejected before T*k
     assert L.moe_workspace_bytes(ctypes.byref(dims(T=0))) >= 256         # T = 0 is valid
     big = dims(T=16384, d=7680, E=256, k=8, f=2048, S=1, f_s=2048, dtype=N.MOE_BF16)
     nb = L.moe_workspace_bytes(ctypes.byref(big))
