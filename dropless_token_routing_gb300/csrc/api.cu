@@ -195,9 +195,9 @@ int run_router(const void* x, const float* w_r, const moe_dims* d, float* logits
 }
 
 // MOE_REARRANGE_GATHER on the bf16 dropless path fuses the rearrangement into the expert
-// GEMMs: their routed token operands are gathered from x / dy by row_src (TMA row gathers),
-// so x_perm and dy_perm are never materialised. fp32 (SIMT kernels) and drop-and-pad (zero
-// padding rows) always keep the rearranged copies.
+// GEMMs: their routed token operands are gathered from x / dy by row_src (16-byte cp.async
+// row copies in the tiles' swizzled layout), so x_perm and dy_perm are never materialised.
+// fp32 (SIMT kernels) and drop-and-pad (zero padding rows) always keep the rearranged copies.
 bool fused_gather(const moe_dims* d) {
   return (d->rearrange & MOE_REARRANGE_GATHER) && d->dtype == MOE_BF16 && d->capacity == 0;
 }
