@@ -15,7 +15,10 @@ fails at least one of them:
 * central finite differences of the forward, for every input entry;
 * torch autograd (fp64) of a dense masked formulation;
 * dgate = <dY_t, Y_q> and the invariances under token permutation and
-  expert relabelling.
+  expert relabelling;
+* the SwiGLU derivative against central differences and the identity
+  silu(a) - silu(-a) = a; the drop-and-pad rows against the dropless
+  permutation cut at the capacity.
 """
 import json
 import math
@@ -499,3 +502,44 @@ def test_capacity_backward_central_differences():
         assert rel < 1e-6, (name, rel)
     # a dropped copy has no gate gradient
     assert np.all(bwd["dgate"].reshape(-1)[fwd["dest"] < 0] == 0)
+
+
+# ---------------------------------------------------------------- helpers pinned directly
+def test_silu_grad_is_the_derivative_of_silu():
+    """silu'(a) against central differences of silu, at 0 (1/2), far out (0 and 1), and the
+    identity silu(a) - silu(-a) = a, whose derivative gives silu'(a) + silu'(-a) = 1."""
+    a = np.linspace(-12.0, 12.0, 481)
+    h = 1e-5
+    fd = (O.silu(a + h) - O.silu(a - h)) / (2 * h)
+    assert np.max(np.abs(O.silu_grad(a) - fd)) < 1e-9
+    assert O.silu_grad(np.array([0.0]))[0] == 0.5
+    assert abs(O.silu_grad(np.array([40.0]))[0] - 1.0) < 1e-12
+    assert abs(O.silu_grad(np.array([-40.0]))[0]) < 1e-12
+    assert np.max(np.abs(O.silu(a) - O.silu(-a) - a)) < 1e-12
+    assert np.max(np.abs(O.silu_grad(a) + O.silu_grad(-a) - 1.0)) < 1e-12
+
+
+@pytest.mark.parametrize("C", [1, 2, 5, 40])
+def test_capacity_permutation_is_the_dropless_order_cut_at_capacity(C):
+    """The drop-and-pad rows are the dropless permutation's segments cut at C rows: copy q of
+    rank r = dest[q] - offsets[e] in its expert's segment lands at row e*C + r when r < C and
+    is dropped otherwise; each expert's first min(C, count) rows hold the dropless rows'
+    tokens, the rest are padding."""
+    rng = np.random.default_rng(7 + C)
+    T, E, k = 37, 6, 3
+    s = rng.standard_normal((T, E)) + np.array([2.0, 1.0, 0.0, 0.0, -1.0, -3.0])
+    idx, _ = O.route_topk(s, k)
+    dest, row_src = O.permutation(idx, E)
+    counts = O.expert_counts(idx, E)
+    off = O.expert_offsets(counts)
+    flat = idx.reshape(-1)
+    rank = dest - off[flat]
+    dc, rc = O.capacity_permutation(idx, E, C)
+    assert np.array_equal(dc, np.where(rank < C, flat * C + rank, -1))
+    for e in range(E):
+        n = min(C, counts[e])
+        assert np.array_equal(rc[e * C:e * C + n], row_src[off[e]:off[e] + n])
+        assert np.all(rc[e * C + n:(e + 1) * C] == -1)
+    # every kept row is filled by exactly one copy
+    kept = dc[dc >= 0]
+    assert len(np.unique(kept)) == len(kept) == int(np.minimum(counts, C).sum())
