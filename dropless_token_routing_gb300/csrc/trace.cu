@@ -1,4 +1,5 @@
 // Launch tracing (see trace.h): event pairs per launch, summed per phase on read.
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -20,7 +21,7 @@ struct Rec {
 };
 
 std::mutex g_mu;
-bool g_on = false;
+std::atomic<bool> g_on{false};   // read without the lock by every launcher
 std::vector<Rec> g_recs;
 std::vector<cudaEvent_t> g_pool;
 Rec g_open[TP_COUNT];
@@ -39,11 +40,11 @@ cudaEvent_t take_event() {
 
 }  // namespace
 
-bool trace_on() { return g_on; }
+bool trace_on() { return g_on.load(std::memory_order_relaxed); }
 
 void trace_record(int phase, cudaStream_t st, bool begin) {
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_on || phase < 0 || phase >= TP_COUNT) return;
+  if (!g_on.load(std::memory_order_relaxed) || phase < 0 || phase >= TP_COUNT) return;
   if (begin) {
     Rec r{phase, take_event(), nullptr};
     cudaEventRecord(r.a, st);
@@ -72,7 +73,7 @@ int moe_trace_enable(int on) {
   }
   g_recs.clear();
   for (int p = 0; p < TP_COUNT; ++p) g_has_open[p] = false;
-  g_on = on != 0;
+  g_on.store(on != 0, std::memory_order_relaxed);
   return MOE_OK;
 }
 
