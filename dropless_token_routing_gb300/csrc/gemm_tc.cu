@@ -181,27 +181,24 @@ __device__ __forceinline__ void issue_tile_loads(const TcParams& p, const TileCo
       tma3d(b_s, &p.b1, bar, kl, n0, s);
     }
   } else if (MODE == BWD2T) {
+    // the weight operand's four 64-column slabs in one 4-D copy (map4d_slabs)
     const int n0 = tc.ni * BN;
     if (!G.shared) {
       if (!gather) tma2d(a_s, am0, bar, k0, row0 + m0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b0, bar, n0 + 64 * i, k0, G.e);
+      tma4d(b_s, &p.b0, bar, 0, k0, n0 / 64, G.e);
     } else {
       tma2d(a_s, am1, bar, k0, m0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b1, bar, n0 + 64 * i, k0, G.s);
+      tma4d(b_s, &p.b1, bar, 0, k0, n0 / 64, G.s);
     }
   } else if (MODE == BWD1T) {
     const int n0 = tc.ni * BN;
     if (!G.shared) {
       tma2d(a_s, am0, bar, k0, row0 + m0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b0, bar, n0 + 64 * i, k0, G.e);
+      tma4d(b_s, &p.b0, bar, 0, k0, n0 / 64, G.e);
     } else {
       const int kpb = 2 * a.f_s / BK, s = kb / kpb, kl = (kb - s * kpb) * BK;
       tma2d(a_s, am1, bar, kl, s * T + m0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) tma3d(b_s + i * SLAB, &p.b1, bar, n0 + 64 * i, kl, s);
+      tma4d(b_s, &p.b1, bar, 0, kl, n0 / 64, s);
     }
   }
 }
@@ -639,16 +636,16 @@ int launch_tc_grouped(int mode, const GroupedArgs& g, int num_sms, cudaStream_t 
       return launch_mode<FWD2>(p, num_sms, st);
     case BWD2T:
       ok = (g.gather_rows != nullptr || (map2d(&p.a0, g.dy_perm, d, Tk, 64, 128) && map2d(&p.h0, g.dy_perm, d, Tk, 64, 64))) &&
-           map3d(&p.b0, g.w2, f, d, E, 64, 64);
+           map4d_slabs(&p.b0, g.w2, f, d, E, 4);
       if (sh) ok = ok && map2d(&p.a1, g.dy, d, T, 64, 128) && map2d(&p.h1, g.dy, d, T, 64, 64) &&
-                   map3d(&p.b1, g.ws2, fs, d, S, 64, 64);
+                   map4d_slabs(&p.b1, g.ws2, fs, d, S, 4);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<BWD2T>(p, num_sms, st);
     case BWD1T:
       ok = map2d(&p.a0, g.dz, 2 * f, Tk, 64, 128) && map2d(&p.h0, g.dz, 2 * f, Tk, 64, 64) &&
-           map3d(&p.b0, g.w13, d, 2 * f, E, 64, 64);
+           map4d_slabs(&p.b0, g.w13, d, 2 * f, E, 4);
       if (sh) ok = ok && map2d(&p.a1, g.dz_sh, 2 * fs, ST, 64, 128) && map2d(&p.h1, g.dz_sh, 2 * fs, ST, 64, 64) &&
-                   map3d(&p.b1, g.ws13, d, 2 * fs, S, 64, 64);
+                   map4d_slabs(&p.b1, g.ws13, d, 2 * fs, S, 4);
       if (!ok) return MOE_ERR_CUDA;
       return launch_mode<BWD1T>(p, num_sms, st);
     case ROUTER:

@@ -29,6 +29,15 @@ __device__ __forceinline__ void tma3d(uint32_t dst, const CUtensorMap* map, uint
       : "memory");
 }
 
+__device__ __forceinline__ void tma4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                      int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // 16 bytes global -> shared through the LSU (L2 only); `bytes` < 16 zero-fills the rest
 // (0: nothing is read).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes = 16) {
@@ -162,6 +171,23 @@ inline bool map3d(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows,
   const cuuint32_t box[3] = {box_c, box_r, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// An MN-major weight operand [n][rows][cols] read as 64-column slabs: the 4-D view
+// {64, rows, cols / 64, n} (strides: a row, 128 bytes between slabs, a matrix) with box
+// {64, 64, nslab, 1} lands nslab slabs of [64 rows][64 columns] one after the other in shared
+// memory, as nslab 3-D loads of box {64, 64, 1} at column offsets 0, 64, ... would.
+inline bool map4d_slabs(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint64_t n,
+                        uint32_t nslab) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || ptr == nullptr || rows == 0 || cols == 0 || n == 0 || cols % 64 != 0) return false;
+  const cuuint64_t dims[4] = {64, rows, cols / 64, n};
+  const cuuint64_t strides[3] = {cols * 2, 128, cols * rows * 2};
+  const cuuint32_t box[4] = {64, 64, nslab, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
