@@ -166,3 +166,24 @@ def test_noalloc_permute_rejects_bad_calls_before_launching():
     assert call(ok, dev_err=GOOD + 2) == _code("MOE_ERR_MISALIGNED")   # not a 32-bit atomic's word
     assert call(ok, x_perm=BAD) == _code("MOE_ERR_MISALIGNED")
     assert call(ok, dest=None) == _code("MOE_ERR_NULL_POINTER")
+
+
+def test_workspace_grows_with_every_dimension_and_the_capacity_tables():
+    """moe_workspace_bytes is monotone in T, d, f, E, k and the shared experts, and the
+    drop-and-pad variant adds its dropless index tables (two int32 per token copy and the
+    dropless offsets) to permuted buffers of E*C rows."""
+    base = dict(T=1024, d=512, E=16, k=4, f=256, S=1, f_s=256, dtype=N.MOE_BF16)
+
+    def ws(capacity=0, **kw):
+        d = dims(**{**base, **kw})
+        d.capacity = capacity
+        return L.moe_workspace_bytes(ctypes.byref(d))
+
+    w0 = ws()
+    for kw in (dict(T=2048), dict(d=1024), dict(f=512), dict(E=32), dict(k=8), dict(S=2), dict(f_s=512)):
+        assert ws(**kw) > w0, kw
+    Tk = base["T"] * base["k"]
+    # E*C == T*k: the same permuted rows, plus the three dropless tables
+    assert ws(capacity=Tk // base["E"]) >= w0 + 8 * Tk
+    # a larger capacity only adds rows
+    assert ws(capacity=2 * Tk // base["E"]) > ws(capacity=Tk // base["E"])
