@@ -37,7 +37,8 @@
  *    (nothing is launched then), or MOE_ERR_LAUNCH / MOE_ERR_CUDA for a CUDA error.
  *  - Errors found on the device (an expert id out of range, a bounded wait that ran out) are
  *    recorded in an error word inside the workspace; moe_get_device_error reads and clears it.
- *  - T == 0 is a valid no-op.
+ *  - T == 0 is a valid no-op (except in the calls that return balance statistics, whose
+ *    means over the tokens need T >= 1: they reject T == 0 with MOE_ERR_BAD_DIMS).
  *  - bf16 needs d, f, f_s multiples of 64; fp32 needs multiples of 8. E <= 1024, 1 <= k <= min(E, 32).
  */
 #ifndef MOE_GB300_H
